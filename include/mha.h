@@ -1,0 +1,167 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head attention forward.
+ *
+ * The operation (itwiki.kr "멀티 헤드 어텐션", section 수식, and the tensor-shape
+ * table of section 텐서 모양으로 본 계산):
+ *
+ *   [Q | K | V] = X W_qkv + b_qkv                    one fused projection
+ *   head_i      = softmax(Q_i K_i^T / sqrt(d_k) [+ M]) V_i
+ *   Ocat        = Concat(head_1, ..., head_h)        head i at columns i*d_v
+ *   Y           = Ocat W_o + b_o
+ *
+ * Q_i, K_i, V_i are column slices of the projection output ("a head is not a
+ * separate matrix, only a slice of one matrix's output dimension", same
+ * table).  M is the causal mask (-inf for key j > query i; iamjaehka13.blog
+ * "[Deep Learning 5] Attention의 내부 계산", section 9) and/or key padding
+ * (keys j >= L_b excluded; molayo1419.me "MHA란 무엇인가?", pitfall 2).
+ * Cross-attention takes Q from X_q and K, V from X_kv (iamjaehka13.blog,
+ * section 19).
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers, row-major, in the handle's
+ *    dtype (fp32 or bf16) unless stated; kv_lengths is device int32.
+ *  - Strides ("ld*") are in elements.
+ *  - Nothing is allocated, freed or synchronised inside the compute calls;
+ *    every kernel is launched asynchronously on `stream` (a cudaStream_t; NULL
+ *    is the legacy default stream).  All memory is owned by the caller.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing.  Errors found on the device (an out-of-range L_b, a
+ *    pipeline wait that ran out of time) are recorded in a status word kept in
+ *    the workspace; read it with mha_get_status.
+ *  - Outputs must not alias inputs.
+ *  - Every function is thread-compatible: one handle must not be used from
+ *    two host threads at once.
+ */
+#ifndef MHA_H_
+#define MHA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mha_s* mha_t; /* opaque; holds the layer configuration only */
+
+typedef enum {
+    MHA_F32 = 0,  /* fp32 storage, fp32 arithmetic (CUDA-core FFMA) */
+    MHA_BF16 = 1  /* bf16 storage, fp32 accumulation (tcgen05 tensor cores) */
+} mha_dtype;
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1, /* a size, pointer, stride or flag is invalid */
+    MHA_ERR_UNSUPPORTED = 2, /* valid, but this build has no kernel for it */
+    MHA_ERR_WORKSPACE = 3,   /* no workspace set, or it is too small */
+    MHA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+    MHA_ERR_TIMEOUT = 5,     /* device status: a pipeline wait gave up */
+    MHA_ERR_BAD_LENGTH = 6   /* device status: some L_b outside [1, T_kv]; its rows are NaN */
+} mha_status;
+
+/*
+ * mha_create -- make a handle for one layer shape.
+ *   D    model width (d_model);  h  number of heads;
+ *   d_k  query/key width per head;  d_v  value width per head
+ *   (itwiki.kr "멀티 헤드 어텐션", 수식: W_i^Q, W_i^K in R^{d_model x d_k},
+ *   W_i^V in R^{d_model x d_v}, W^O in R^{h d_v x d_model}).
+ * Any positive D, h, d_k, d_v is accepted here; a dtype/shape pair without a
+ * kernel is reported by the compute calls as MHA_ERR_UNSUPPORTED.
+ * Returns MHA_ERR_INVALID_ARG for out == NULL or a non-positive size, and
+ * MHA_ERR_CUDA if no CUDA device can be queried.  Host memory only.
+ */
+mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype);
+
+/* mha_destroy -- free the handle (NULL is ignored).  Does not touch the
+ * caller's workspace. */
+void mha_destroy(mha_t handle);
+
+/*
+ * mha_workspace_size -- bytes of device workspace mha_forward needs for
+ * batch B, T_q query rows and T_kv key rows (self-attention: T_kv = T_q).
+ * Layout: a 256-byte status block, the projected Q (B,T_q,h*d_k) and K,V
+ * (B,T_kv,h*(d_k+d_v)) -- for self-attention one (B,T,2h*d_k+h*d_v) buffer
+ * -- and Ocat (B,T_q,h*d_v), each 256-byte aligned.  Returns 0 for an invalid
+ * handle or size.
+ */
+size_t mha_workspace_size(mha_t handle, int B, int T_q, int T_kv);
+
+/*
+ * mha_set_workspace -- attach caller-owned device memory (256-byte aligned,
+ * `bytes` long) to the handle, and zero its status block (a synchronous
+ * cudaMemset of 256 bytes).  The memory must stay valid while calls using
+ * the handle are in flight.  NULL detaches.
+ */
+mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes);
+
+/*
+ * mha_forward -- Y = MultiHead(X_q, X_kv) for the whole batch.
+ *   X_q    (B, T_q, D)
+ *   X_kv   (B, T_kv, D); NULL or == X_q means self-attention (T_kv must equal
+ *          T_q), done with ONE fused GEMM against all of W_qkv
+ *   W_qkv  (D, 2*h*d_k + h*d_v), column blocks [W^Q | W^K | W^V]; head i of
+ *          each block is its columns [i*d, (i+1)*d)
+ *   b_qkv  (2*h*d_k + h*d_v) or NULL
+ *   W_o    (h*d_v, D);  b_o  (D) or NULL
+ *   causal nonzero applies the causal mask (key j > query i excluded);
+ *          requires T_q == T_kv
+ *   kv_lengths  device int32[B] or NULL; keys j >= kv_lengths[b] excluded.
+ *          Values outside [1, T_kv] make that batch's output NaN and record
+ *          MHA_ERR_BAD_LENGTH in the status word (an all-masked softmax row is
+ *          undefined, molayo1419.me pitfall 3)
+ *   out    (B, T_q, D)
+ * Needs a workspace of mha_workspace_size(B, T_q, T_kv) bytes.  Launches
+ * three kernels (self) or four (cross) on `stream`.
+ * bf16 requires d_k == d_v in {64, 128}, D and h*d_k multiples of 64 and
+ * 16-byte aligned pointers (else MHA_ERR_UNSUPPORTED / MHA_ERR_INVALID_ARG);
+ * fp32 accepts any shape with d_k, d_v <= 256.
+ */
+mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                       const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                       int causal, const int32_t* kv_lengths, void* out, void* stream);
+
+/*
+ * mha_linear -- one projection step, C = A W + bias
+ * (itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영).
+ *   A (M, K) row stride lda;  W (K, N) row stride ldw;  bias (N) or NULL;
+ *   C (M, N) row stride ldc.   fp32 accumulate in both dtypes.
+ * bf16 requires K, N, lda, ldw, ldc multiples of 8 and 16-byte aligned
+ * pointers.  M, N, K >= 1.
+ */
+mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K,
+                      const void* W, int64_t ldw, int N, const void* bias,
+                      void* C, int64_t ldc, void* stream);
+
+/*
+ * mha_attention -- the fused attention step for all heads: scores, scale,
+ * mask, row softmax and weighted sum, written straight into the
+ * concatenated layout (itwiki.kr "멀티 헤드 어텐션", table rows 헤드 분리
+ * through 헤드 결합).  The (B,h,T_q,T_kv) scores never reach memory.
+ *   Q  rows (B, T_q) of stride ldq; head i reads columns [i*d_k, (i+1)*d_k)
+ *   K  rows (B, T_kv) of stride ldk; head i reads columns [i*d_k, (i+1)*d_k)
+ *   V  rows (B, T_kv) of stride ldv; head i reads columns [i*d_v, (i+1)*d_v)
+ *   O  rows (B, T_q) of stride ldo; head i writes columns [i*d_v, (i+1)*d_v)
+ * causal / kv_lengths as for mha_forward.  The head split is this strided
+ * addressing: the projection output is read in place, never copied.
+ */
+mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv,
+                         const void* Q, int64_t ldq, const void* K, int64_t ldk,
+                         const void* V, int64_t ldv, int causal, const int32_t* kv_lengths,
+                         void* O, int64_t ldo, void* stream);
+
+/*
+ * mha_get_status -- copy the device status word of the attached workspace to
+ * *status_out (an mha_status: MHA_OK, MHA_ERR_TIMEOUT or MHA_ERR_BAD_LENGTH;
+ * the first error recorded wins) and reset it to MHA_OK.  Synchronises
+ * `stream`.  Returns MHA_ERR_WORKSPACE if no workspace is attached.
+ */
+mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream);
+
+/* mha_strerror -- static description of a status code. */
+const char* mha_strerror(mha_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_H_ */

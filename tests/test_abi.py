@@ -1,0 +1,105 @@
+"""The C-ABI library: it loads, exports every function include/mha.h declares,
+and rejects bad arguments on the host before touching the GPU.  No test here
+launches a kernel, so the file runs on a machine without a GPU."""
+import ctypes
+
+import pytest
+
+from transformer_head_scaled_02_gb300 import _lib as L
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build_library()
+    return L.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = L.header_symbols()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_every_code(lib):
+    for code in range(7):
+        assert L.strerror(code) not in ("", "unknown status")
+    assert L.strerror(99) == "unknown status"
+
+
+def test_create_rejects_bad_sizes(lib):
+    h = ctypes.c_void_p()
+    for args in ((0, 8, 64, 64, 1), (512, 0, 64, 64, 1), (512, 8, -1, 64, 1),
+                 (512, 8, 64, 0, 1), (512, 8, 64, 64, 7)):
+        assert lib.mha_create(ctypes.byref(h), *args) == L.MHA_ERR_INVALID_ARG
+    assert lib.mha_create(None, 512, 8, 64, 64, 1) == L.MHA_ERR_INVALID_ARG
+
+
+def test_workspace_size_layout(lib):
+    hdl = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    try:
+        # status 256 + Q (B*T*D*2) + KV (B*T*2D*2) + Ocat (B*T*D*2), each 256-aligned
+        B, T, D = 4, 2048, 1024
+        assert L.mha_workspace_size(hdl, B, T, T) == 256 + B * T * D * 2 * 4
+        assert L.mha_workspace_size(hdl, -1, T, T) == 0
+        assert L.mha_workspace_size(None, 1, 1, 1) == 0
+    finally:
+        L.mha_destroy(hdl)
+
+
+def test_forward_rejects_bad_arguments_before_any_launch(lib):
+    bf = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    f32 = L.mha_create(64, 2, 32, 32, L.MHA_F32)
+    odd = L.mha_create(96, 3, 32, 32, L.MHA_BF16)   # d_k = 32: no tensor-core kernel
+    fake = 1 << 40                                   # never dereferenced: rejected earlier
+    try:
+        def fwd(h, **kw):
+            a = dict(X_q=fake, X_kv=None, B=2, T_q=128, T_kv=128, W_qkv=fake, b_qkv=None,
+                     W_o=fake, b_o=None, causal=0, kv_lengths=None, out=fake + (1 << 30),
+                     stream=None)
+            a.update(kw)
+            return L.mha_forward(h, check=False, **a)
+        assert fwd(None) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, B=-1) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, causal=1, X_kv=fake + (1 << 32), T_kv=256) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, T_kv=64) == L.MHA_ERR_INVALID_ARG          # self-attention needs T_kv == T_q
+        assert fwd(bf, X_q=None) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, W_o=None) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, out=None) == L.MHA_ERR_INVALID_ARG
+        assert fwd(bf, out=fake) == L.MHA_ERR_INVALID_ARG          # output aliases X_q
+        assert fwd(bf, X_q=fake + 2) == L.MHA_ERR_INVALID_ARG      # bf16 needs 16-byte alignment
+        assert fwd(bf) == L.MHA_ERR_WORKSPACE                       # no workspace attached
+        assert fwd(odd) == L.MHA_ERR_UNSUPPORTED
+        assert fwd(f32, X_q=fake + 4) == L.MHA_ERR_WORKSPACE        # fp32: no alignment rule
+        assert fwd(bf, B=0) == L.MHA_OK                             # empty batch: nothing to do
+        assert fwd(bf, T_q=0, T_kv=0) == L.MHA_OK
+        assert fwd(bf, X_kv=fake + (1 << 32), T_kv=0) == L.MHA_ERR_INVALID_ARG
+    finally:
+        for h in (bf, f32, odd):
+            L.mha_destroy(h)
+
+
+def test_linear_and_attention_reject_bad_arguments(lib):
+    bf = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    fake = 1 << 40
+    try:
+        lin = lambda **kw: L.mha_linear(bf, **{**dict(A=fake, lda=64, M=10, K=64, W=fake + (1 << 30),
+                                                      ldw=64, N=64, bias=None, C=fake + (1 << 32),
+                                                      ldc=64, stream=None), **kw}, check=False)
+        assert lin(K=0) == L.MHA_ERR_INVALID_ARG
+        assert lin(K=60, lda=60) == L.MHA_ERR_INVALID_ARG           # bf16: K % 8
+        assert lin(lda=32) == L.MHA_ERR_INVALID_ARG                 # lda < K
+        assert lin(C=fake) == L.MHA_ERR_INVALID_ARG                 # C aliases A
+        assert lin(M=0) == L.MHA_OK
+        att = lambda **kw: L.mha_attention(bf, **{**dict(B=1, T_q=10, T_kv=10, Q=fake, ldq=3072,
+                                                         K=fake + 2048, ldk=3072, V=fake + 4096,
+                                                         ldv=3072, causal=0, kv_lengths=None,
+                                                         O=fake + (1 << 32), ldo=1024,
+                                                         stream=None), **kw}, check=False)
+        assert att(ldq=1000) == L.MHA_ERR_INVALID_ARG               # < h*d_k
+        assert att(causal=1, T_kv=11) == L.MHA_ERR_INVALID_ARG
+        assert att(O=None) == L.MHA_ERR_INVALID_ARG
+        assert att(T_q=0) == L.MHA_OK
+    finally:
+        L.mha_destroy(bf)

@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.
+
+  * single steps: the projection GEMM (mha_linear) and the fused attention
+    (mha_attention) against the oracle's linear / attention steps, element by
+    element, over shapes that span several tiles and a ragged tail;
+  * the whole forward (mha_forward) on small shapes, element by element,
+    including cross-attention with key padding, d = 64 and 128, fp32 and bf16;
+  * the five named workloads at full size: the fp32 ones element by element,
+    the bf16 ones on sampled query rows (tile edges, first and last rows) that
+    the oracle computes one by one;
+  * edge cases: empty batch, one query row, one valid key, invalid lengths
+    (NaN rows and a device status), guard bands around the output, padding
+    invariance, determinism.
+Tolerances are those of tests/gpu_util.py.
+"""
+import numpy as np
+import pytest
+
+from gpu_util import assert_close, errors, to_device, to_host, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from transformer_head_scaled_02_gb300 import Mha  # noqa: E402
+from transformer_head_scaled_02_gb300 import _lib  # noqa: E402
+from transformer_head_scaled_02_gb300 import workloads as wl  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+
+
+def _layer(w):
+    return Mha(w.D, w.h, w.d_k, w.d_v, dtype=torch_dtype(w.dtype))
+
+
+def _run_forward(w, x, layer=None):
+    layer = layer or _layer(w)
+    d = {k: to_device(v, w.dtype) for k, v in x.items() if k != "kv_lengths"}
+    kvl = None if x["kv_lengths"] is None else torch.from_numpy(x["kv_lengths"]).cuda()
+    y = layer.forward(d["X_q"], d["W_qkv"], d["b_qkv"], d["W_o"], d["b_o"], X_kv=d["X_kv"],
+                      causal=w.causal, kv_lengths=kvl)
+    torch.cuda.synchronize()
+    return layer, y
+
+
+def _oracle_forward(w, x, rows=None):
+    return oracle.mha_forward(x["X_q"], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h, w.d_k,
+                              w.d_v, Xkv=x["X_kv"], causal=w.causal, kv_lengths=x["kv_lengths"],
+                              rows=rows)
+
+
+# ------------------------------------------------------------------ step: projection GEMM
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("M,K,N,bias", [
+    (1, 64, 64, True),          # one row
+    (300, 1024, 3072, True),    # ragged M, several N tiles
+    (257, 72, 200, False),      # K tail inside a 64-wide block, N tail inside a 256-wide tile
+    (1024, 512, 1536, True),
+])
+def test_linear_step(dtype, M, K, N, bias):
+    A = wl.random_tensor((M, K), seed=1, dtype=dtype)
+    W = wl.random_tensor((K, N), seed=2, dtype=dtype, scale=0.05)
+    b = wl.random_tensor((N,), seed=3, dtype=dtype, scale=0.1) if bias else None
+    layer = Mha(64, 1, 64, dtype=torch_dtype(dtype))
+    C = layer.linear(to_device(A, dtype), to_device(W, dtype), to_device(b, dtype))
+    torch.cuda.synchronize()
+    assert_close(to_host(C), oracle.linear(A, W, b), dtype, f"linear {M}x{K}x{N}")
+
+
+def test_linear_strided_operands():
+    """Row strides wider than the rows (a column block of W_qkv, as the
+    cross-attention path uses)."""
+    M, K, N, ld = 200, 128, 192, 576
+    A = wl.random_tensor((M, K), seed=4)
+    Wfull = wl.random_tensor((K, ld), seed=5, scale=0.05)
+    layer = Mha(64, 1, 64, dtype=torch.bfloat16)
+    Wd = to_device(Wfull, "bf16")
+    out = torch.zeros((M, ld), dtype=torch.bfloat16, device="cuda")
+    layer.linear(to_device(A, "bf16"), Wd[:, 192:384], None, out=out[:, 64:256])
+    torch.cuda.synchronize()
+    ref = oracle.linear(A, Wfull[:, 192:384])
+    assert_close(to_host(out[:, 64:256]), ref, "bf16", "strided linear")
+    assert (to_host(out[:, :64]) == 0).all() and (to_host(out[:, 256:]) == 0).all()
+
+
+# ------------------------------------------------------------------ step: fused attention
+
+ATTN_CASES = [
+    # B, T_q, T_kv, h, d, causal, lengths, scale
+    (1, 128, 128, 1, 64, False, None, 1.0),
+    (2, 200, 200, 3, 64, True, None, 1.0),
+    (1, 129, 129, 2, 128, True, None, 1.0),
+    (2, 127, 127, 2, 128, False, None, 1.0),
+    (1, 1, 1, 2, 64, True, None, 1.0),                     # one query, one key
+    (3, 70, 333, 2, 64, False, [1, 200, 333], 1.0),        # cross + padding incl. L=1, L=T_kv
+    (2, 300, 300, 2, 64, True, [300, 129], 1.0),           # causal + padding
+    (1, 384, 384, 2, 64, True, None, 4.0),                 # large scores: rescale path
+    (2, 256, 520, 1, 128, False, [520, 257], 3.0),
+]
+
+
+@pytest.mark.parametrize("B,T_q,T_kv,h,d,causal,lengths,scale", ATTN_CASES)
+def test_attention_step_bf16(B, T_q, T_kv, h, d, causal, lengths, scale):
+    Q = wl.random_tensor((B, T_q, h * d), seed=10, scale=scale)
+    K = wl.random_tensor((B, T_kv, h * d), seed=11, scale=scale)
+    V = wl.random_tensor((B, T_kv, h * d), seed=12)
+    kvl = None if lengths is None else np.array(lengths, dtype=np.int32)
+    layer = Mha(h * d, h, d, dtype=torch.bfloat16)
+    layer.ensure_workspace(1, 1, 1)
+    O = layer.attention(to_device(Q, "bf16"), to_device(K, "bf16"), to_device(V, "bf16"),
+                        causal=causal,
+                        kv_lengths=None if kvl is None else torch.from_numpy(kvl).cuda())
+    torch.cuda.synchronize()
+    assert layer.status() == _lib.MHA_OK
+    ref = oracle.attention(Q, K, V, h=h, causal=causal, kv_lengths=kvl)
+    assert_close(to_host(O), ref, "bf16", f"attention {B}x{T_q}x{T_kv} h{h} d{d}")
+
+
+@pytest.mark.parametrize("B,T_q,T_kv,h,dk,dv,causal,lengths", [
+    (1, 16, 16, 8, 4, 4, False, None),
+    (2, 77, 77, 3, 16, 8, True, None),
+    (2, 40, 90, 2, 64, 96, False, [1, 90]),
+    (1, 33, 33, 1, 256, 256, True, None),
+])
+def test_attention_step_f32(B, T_q, T_kv, h, dk, dv, causal, lengths):
+    Q = wl.random_tensor((B, T_q, h * dk), seed=20, dtype="f32")
+    K = wl.random_tensor((B, T_kv, h * dk), seed=21, dtype="f32")
+    V = wl.random_tensor((B, T_kv, h * dv), seed=22, dtype="f32")
+    kvl = None if lengths is None else np.array(lengths, dtype=np.int32)
+    layer = Mha(h * dk, h, dk, dv, dtype=torch.float32)
+    O = layer.attention(to_device(Q, "f32"), to_device(K, "f32"), to_device(V, "f32"),
+                        causal=causal,
+                        kv_lengths=None if kvl is None else torch.from_numpy(kvl).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.attention(Q, K, V, h=h, causal=causal, kv_lengths=kvl)
+    assert_close(to_host(O), ref, "f32", "f32 attention")
+
+
+# ------------------------------------------------------------------ whole forward, small
+
+SMALL = [
+    wl.custom("bf16_d64_causal", B=2, T_q=300, D=256, h=4, d_k=64, causal=True),
+    wl.custom("bf16_d128_causal", B=1, T_q=260, D=512, h=4, d_k=128, causal=True),
+    wl.custom("bf16_d64_full", B=3, T_q=129, D=192, h=3, d_k=64, causal=False, bias="none"),
+    wl.custom("bf16_cross_pad", B=3, T_q=100, T_kv=333, D=256, h=4, d_k=64, cross=True,
+              kv_len_range=(1, 333)),
+    wl.custom("bf16_cross_d128", B=2, T_q=64, T_kv=200, D=256, h=2, d_k=128, cross=True,
+              kv_len_range=(100, 200), bias="none"),
+    wl.custom("f32_odd", B=2, T_q=37, D=48, h=3, d_k=16, d_v=8, dtype="f32", causal=True,
+              weight_init="xavier_uniform", bias="uniform_0.1"),
+    wl.custom("f32_cross", B=2, T_q=20, T_kv=45, D=64, h=4, d_k=16, dtype="f32", cross=True,
+              kv_len_range=(1, 45), weight_init="uniform_inv_sqrt_d", bias="uniform_0.1"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_forward_small(w):
+    x = wl.make_inputs(w, seed=3)
+    layer, y = _run_forward(w, x)
+    assert layer.status() == _lib.MHA_OK
+    assert_close(to_host(y), _oracle_forward(w, x), w.dtype, w.name)
+
+
+# ------------------------------------------------------------------ named workloads, full size
+
+@pytest.mark.parametrize("name", ["c1_f32_tiny", "c2_f32_causal"])
+def test_named_f32_full(name):
+    w = wl.WORKLOADS[name]
+    x = wl.make_inputs(w)
+    layer, y = _run_forward(w, x)
+    assert layer.status() == _lib.MHA_OK
+    e = assert_close(to_host(y), _oracle_forward(w, x), "f32", name)
+    print(name, e)
+
+
+SAMPLED_ROWS = {
+    "c3_bf16_causal": [0, 1, 127, 128, 129, 1000, 2046, 2047],
+    "c4_bf16_causal_long": [0, 1, 127, 128, 8191, 16383],
+    "c5_bf16_cross": [0, 1, 127, 255, 511],
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLED_ROWS))
+def test_named_bf16_full_sampled_rows(name):
+    """The full-size workload through mha_forward (as the benchmark runs it);
+    the oracle computes the sampled query rows of every batch one by one."""
+    w = wl.WORKLOADS[name]
+    x = wl.make_inputs(w)
+    layer, y = _run_forward(w, x)
+    assert layer.status() == _lib.MHA_OK
+    rows = SAMPLED_ROWS[name]
+    got = to_host(y[:, rows, :])
+    ref = _oracle_forward(w, x, rows=rows)
+    e = assert_close(got, ref, "bf16", name)
+    print(name, e)
+    # properties that hold at any size, over every row: finite, and not all equal
+    yy = y.float()
+    assert torch.isfinite(yy).all()
+    assert float(yy.std()) > 0
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_invalid_lengths_give_nan_rows_and_status():
+    """molayo1419.me pitfall 3: a sample whose keys are all excluded has an
+    undefined softmax; its rows come out NaN and the call reports it."""
+    for dtype in ("bf16", "f32"):
+        w = wl.custom("badlen", B=3, T_q=50, T_kv=140, D=128, h=2, d_k=64, cross=True,
+                      kv_len_range=(1, 140), dtype=dtype)
+        x = wl.make_inputs(w, seed=5)
+        x["kv_lengths"] = np.array([0, 77, 141], dtype=np.int32)
+        layer, y = _run_forward(w, x)
+        assert layer.status() == _lib.MHA_ERR_BAD_LENGTH
+        assert layer.status() == _lib.MHA_OK  # reading clears it
+        yh = to_host(y)
+        assert np.isnan(yh[0]).all() and np.isnan(yh[2]).all()
+        ref = _oracle_forward(w, {**x, "kv_lengths": np.array([1, 77, 1], dtype=np.int32)})
+        assert_close(yh[1], ref[1], dtype, "valid batch next to invalid ones")
+
+
+def test_padding_rows_do_not_matter_and_runs_are_deterministic():
+    w = wl.custom("padinv", B=2, T_q=64, T_kv=300, D=256, h=4, d_k=64, cross=True,
+                  kv_len_range=(130, 250))
+    x = wl.make_inputs(w, seed=6)
+    layer, y1 = _run_forward(w, x)
+    _, y1b = _run_forward(w, x, layer)
+    assert torch.equal(y1, y1b)
+    x2 = dict(x)
+    xkv = x["X_kv"].copy()
+    for b, L in enumerate(x["kv_lengths"]):
+        xkv[b, L:] = wl.round_to_bf16(np.full_like(xkv[b, L:], 30.0))
+    x2["X_kv"] = xkv
+    _, y2 = _run_forward(w, x2, layer)
+    assert torch.equal(y1, y2)
+
+
+def test_output_guard_bands_untouched():
+    w = wl.custom("guard", B=2, T_q=131, D=256, h=4, d_k=64, causal=True)
+    x = wl.make_inputs(w, seed=7)
+    layer = _layer(w)
+    d = {k: to_device(v, w.dtype) for k, v in x.items() if k != "kv_lengths"}
+    n = w.B * w.T_q * w.D
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[pad:pad + n].view(w.B, w.T_q, w.D)
+    layer.forward(d["X_q"], d["W_qkv"], d["b_qkv"], d["W_o"], d["b_o"], causal=True, out=out)
+    torch.cuda.synchronize()
+    assert (buf[:pad] == 12345.0).all() and (buf[pad + n:] == 12345.0).all()
+    assert_close(to_host(out), _oracle_forward(w, x), "bf16", "guard")
+
+
+def test_empty_batch_is_a_no_op():
+    layer = Mha(256, 4, 64, dtype=torch.bfloat16)
+    X = torch.empty((0, 10, 256), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((256, 768), dtype=torch.bfloat16, device="cuda")
+    Wo = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    y = layer.forward(X, W, None, Wo, None)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 10, 256)

@@ -1,0 +1,293 @@
+// gemm_bf16.cu -- the projection steps on tcgen05 tensor cores:
+//   C = A W + bias    (A (M,K) bf16, W (K,N) bf16 (in,out) row-major, fp32 accumulate, C bf16)
+// which is [Q|K|V] = X W_qkv + b_qkv and Y = Ocat W_o + b_o of
+// itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영.
+//
+// Design (persistent, warp-specialised, one CTA per SM):
+//   warp 0      TMA producer: A tile 128x64 (K-major, 128B swizzle) and W tile 64x256
+//               (N-major: four 64x64 boxes) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N=256, K=16)
+//               from one thread; accumulators double-buffered in TMEM (2 x 256 columns) so
+//               the epilogue of tile i overlaps the main loop of tile i+1;
+//   warps 2..5  epilogue: tcgen05.ld the fp32 accumulator (one TMEM lane = one output row),
+//               add bias, round to bf16, stage 32x64 sub-tiles in swizzled shared memory
+//               and write them with TMA stores (double-buffered per warp).
+// W stays in its natural (in,out) layout: the MMA reads it as an MN-major operand, so no
+// transpose pass over the weights is needed.  Ragged M, N, K are handled by TMA bounds
+// (zero fill on loads, clipping on stores).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int G_BM = 128;
+constexpr int G_BN = 256;
+constexpr int G_BK = 64;
+constexpr int G_STAGES = 4;
+constexpr int G_A_BYTES = G_BM * G_BK * 2;  // 16 KB
+constexpr int G_B_CHUNK = G_BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-columns
+constexpr int G_B_BYTES = G_BK * G_BN * 2;  // 32 KB
+constexpr int G_EPI_BUF = 32 * 64 * 2;      // 4 KB: 32 rows x 64 columns
+constexpr int G_EPI_BYTES = 4 * 2 * G_EPI_BUF;
+constexpr int G_BAR_BYTES = 256;
+constexpr int G_SMEM = G_STAGES * (G_A_BYTES + G_B_BYTES) + G_EPI_BYTES + G_BAR_BYTES + 1024;
+constexpr int G_THREADS = 192;
+constexpr uint32_t G_TMEM_COLS = 512;
+
+static_assert(G_SMEM <= 232448, "shared memory budget");
+
+// Bounded wait that ignores the abort flag: used only to drain copies / MMAs still in
+// flight before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__global__ void __launch_bounds__(G_THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __nv_bfloat16* __restrict__ bias, int M, int N, int K,
+                        int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + G_STAGES * G_A_BYTES;
+    const uint32_t sE = sB + G_STAGES * G_B_BYTES;
+    const uint32_t sBar = sE + G_EPI_BYTES;
+    // barrier layout: full[S], empty[S], tfull[2], tempty[2], mma_drain
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8u * G_STAGES;
+    const uint32_t bar_tfull = sBar + 16u * G_STAGES;
+    const uint32_t bar_tempty = bar_tfull + 16u;
+    const uint32_t bar_drain = bar_tempty + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (M + G_BM - 1) / G_BM;
+    const int num_n = (N + G_BN - 1) / G_BN;
+    const int num_tiles = num_m * num_n;
+    const int num_k = (K + G_BK - 1) / G_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8u * a, 1);
+            mbar_init(bar_tempty + 8u * a, 128);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), G_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % num_m) * G_BM;
+                const int n0 = (tile / num_m) * G_BN;
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full + 8u * stage;
+                    mbar_arrive_expect_tx(fb, G_A_BYTES + G_B_BYTES);
+                    tma_load_2d(sA + stage * G_A_BYTES, &tmA, kb * G_BK, m0, fb);
+#pragma unroll
+                    for (int c = 0; c < G_BN / 64; ++c)
+                        tma_load_2d(sB + stage * G_B_BYTES + c * G_B_CHUNK, &tmW, n0 + c * 64,
+                                    kb * G_BK, fb);
+                    ++issued;
+                    if (++stage == G_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every load issued must have landed before the CTA exits (on the normal path
+            // these phases completed long ago and the waits return at once).
+            for (int back = 0; back < G_STAGES && back < issued; ++back) {
+                stage = stage == 0 ? G_STAGES - 1 : stage - 1;
+                if (stage == G_STAGES - 1) phase ^= 1u;
+                drain_wait(bar_full + 8u * stage, phase);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(G_BM, G_BN, false, true);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(bar_tempty + 8u * acc, acc_phase ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G_BN);
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_full + 8u * stage, phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * G_A_BYTES;
+                    const uint32_t b0 = sB + stage * G_B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < G_BK / 16; ++k) {
+                        const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(b0 + k * 2048, G_B_CHUNK, 1024);
+                        mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar_empty + 8u * stage);
+                    if (++stage == G_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar_tfull + 8u * acc);
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            tc_commit(bar_drain);
+            drain_wait(bar_drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, one TMEM lane (= output row) per thread
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int e = warp - 2;  // staging-buffer owner index
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint32_t bufsel = 0;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int m0 = (tile % num_m) * G_BM;
+            const int n0 = (tile / num_m) * G_BN;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
+                break;
+            tc_fence_after();
+            const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
+#pragma unroll 1
+            for (int c = 0; c < G_BN / 64; ++c) {
+                uint32_t v[2][32];
+                tmem_ld32(t0 + c * 64, v[0]);
+                tmem_ld32(t0 + c * 64 + 32, v[1]);
+                tmem_wait_ld();
+                if (c == G_BN / 64 - 1) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    mbar_arrive(bar_tempty + 8u * acc);
+                }
+                const int nc = n0 + c * 64;
+                if (nc >= N || m0 + q * 32 >= M) continue;  // sub-tile wholly outside C
+                const uint32_t buf = sE + (uint32_t)((e * 2 + (int)bufsel) * G_EPI_BUF);
+                if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
+                __syncwarp();
+                const uint32_t row = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
+                    if (bias != nullptr && nc + u * 8 < N) {
+                        const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
+                        const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            x[2 * i] += __uint_as_float(bw[i] << 16);
+                            x[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
+                        }
+                    }
+                    st_shared_v4(row + ((uint32_t)(u ^ (lane & 7)) << 4), pack_bf16x2(x[0], x[1]),
+                                 pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                                 pack_bf16x2(x[6], x[7]));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmC, buf, nc, m0 + q * 32);
+                    bulk_commit_group();
+                }
+                bufsel ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, G_TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
+                             const void* bias, void* C, int64_t ldc, int M, int N, int K,
+                             int num_sms, int* status, cudaStream_t stream) {
+    CUtensorMap tA, tW, tC;
+    {
+        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)lda * 2};
+        const uint32_t box[2] = {64, G_BM};
+        if (!encode_tmap_bf16(&tA, A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)N, (uint64_t)K};
+        const uint64_t strides[1] = {(uint64_t)ldw * 2};
+        const uint32_t box[2] = {64, G_BK};
+        if (!encode_tmap_bf16(&tW, W, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)N, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)ldc * 2};
+        const uint32_t box[2] = {64, 32};
+        if (!encode_tmap_bf16(&tC, C, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t err = cudaFuncSetAttribute(gemm_bf16_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+    if (err != cudaSuccess) return err;
+    const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
+    const int grid = num_tiles < num_sms ? num_tiles : num_sms;
+    gemm_bf16_tc_kernel<<<grid, G_THREADS, G_SMEM, stream>>>(
+        tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
+    return cudaGetLastError();
+}
+
+}  // namespace mha

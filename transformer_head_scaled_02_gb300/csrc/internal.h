@@ -1,0 +1,40 @@
+// internal.h -- host-side declarations shared by the kernel translation units and the
+// C-ABI layer.  Not part of the public interface (that is include/mha.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mha {
+
+// Encode a bf16 tiled tensor map with 128-byte swizzle and zero fill out of bounds.
+// dims[0] is the innermost (contiguous) extent; strides_bytes has rank-1 entries.
+// Returns false if the driver entry point is unavailable or rejects the map.
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
+
+// C = A W + bias, fp32 everywhere.  A (M,K) lda; W (K,N) ldw; C (M,N) ldc.
+cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t ldw,
+                            const float* bias, float* C, int64_t ldc, int M, int N, int K,
+                            cudaStream_t stream);
+
+// Attention for all heads, fp32.  See mha_attention in include/mha.h for the layout.
+cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,
+                            const float* V, int64_t ldv, float* O, int64_t ldo, int B, int h,
+                            int T_q, int T_kv, int d_k, int d_v, int causal,
+                            const int32_t* kv_lengths, int* status, cudaStream_t stream);
+
+// C = A W + bias on tcgen05: bf16 operands, fp32 accumulation in TMEM, bf16 output.
+// Requires K, N, lda, ldw, ldc multiples of 8 and 16-byte aligned pointers.
+cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
+                             const void* bias, void* C, int64_t ldc, int M, int N, int K,
+                             int num_sms, int* status, cudaStream_t stream);
+
+// Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v).
+cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t ldk,
+                             const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
+                             int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
+                             int* status, cudaStream_t stream);
+
+}  // namespace mha

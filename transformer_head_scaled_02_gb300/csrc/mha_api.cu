@@ -1,0 +1,357 @@
+// mha_api.cu -- the C ABI of include/mha.h: handle, host-side validation, workspace
+// layout and the launch sequence of the forward pass.
+//
+// mha_forward (itwiki.kr "멀티 헤드 어텐션", tensor-shape table, all rows):
+//   self-attention : one GEMM  X (B*T, D) x W_qkv (D, 2h*d_k + h*d_v) -> QKV (B*T, 3D-wide)
+//                    attention reads Q, K, V as strided column views of that buffer
+//                    (the head split is addressing, not a copy) and writes Ocat (B*T, h*d_v)
+//                    GEMM  Ocat x W_o -> Y
+//   cross-attention: GEMM X_q x W_qkv[:, Q block] -> Q; GEMM X_kv x W_qkv[:, K|V blocks] -> KV
+//                    (iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", section 19),
+//                    then attention and the output GEMM as above.
+// All launches go to the caller's stream; nothing is allocated or synchronised here.
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/mha.h"
+#include "internal.h"
+
+struct mha_s {
+    int D, h, dk, dv;
+    mha_dtype dtype;
+    void* ws;
+    size_t ws_bytes;
+};
+
+namespace mha {
+
+// ------------------------------------------------------------------ tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static int g_encode_state = 0;  // 0 unknown, 1 ok, -1 unavailable
+
+static bool get_encoder() {
+    if (g_encode_state == 0) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t err =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn != nullptr) {
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            g_encode_state = 1;
+        } else {
+            g_encode_state = -1;
+        }
+    }
+    return g_encode_state == 1;
+}
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+    if (!get_encoder()) return false;
+    cuuint64_t gdim[5];
+    cuuint64_t gstr[4];
+    cuuint32_t bdim[5];
+    cuuint32_t estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) gstr[i] = strides_bytes[i];
+    }
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                                const_cast<void*>(base), gdim, gstr, bdim, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace mha
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t elem_bytes(mha_dtype t) { return t == MHA_F32 ? 4 : 2; }
+
+// Bytes of [p, p + n) overlap [q, q + m)?
+inline bool overlaps(const void* p, size_t n, const void* q, size_t m) {
+    if (!p || !q || n == 0 || m == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+struct WsLayout {
+    size_t q_off, kv_off, o_off, total;
+};
+
+// status | Q (B,T_q,h*dk) | KV (B,T_kv,h*(dk+dv)) | Ocat (B,T_q,h*dv).  For self-attention the
+// Q and KV regions are used as one fused (B,T,2h*dk+h*dv) buffer starting at q_off, which
+// needs no more bytes than the two regions together.
+WsLayout ws_layout(const mha_s* m, int B, int T_q, int T_kv) {
+    const size_t s = elem_bytes(m->dtype);
+    const size_t hq = (size_t)m->h * m->dk, hv = (size_t)m->h * m->dv;
+    WsLayout w;
+    w.q_off = kStatusBytes;
+    w.kv_off = w.q_off + align256((size_t)B * T_q * hq * s);
+    w.o_off = w.kv_off + align256((size_t)B * T_kv * (hq + hv) * s);
+    w.total = w.o_off + align256((size_t)B * T_q * hv * s);
+    return w;
+}
+
+int g_num_sms = 0;
+int g_num_sms_dev = -1;
+
+mha_status query_sms(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+    if (dev != g_num_sms_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return MHA_ERR_CUDA;
+        g_num_sms = n;
+        g_num_sms_dev = dev;
+    }
+    *out = g_num_sms;
+    return MHA_OK;
+}
+
+// Does this build have tensor-core kernels for the handle's shape?
+bool bf16_shape_supported(const mha_s* m) {
+    return m->dk == m->dv && (m->dk == 64 || m->dk == 128) && (m->D % 8) == 0;
+}
+
+int* status_ptr(const mha_s* m) { return m->ws ? reinterpret_cast<int*>(m->ws) : nullptr; }
+
+// ---------------------------------------------------------------- step launchers (validated)
+
+mha_status run_linear(const mha_s* m, const void* A, int64_t lda, int M, int K, const void* W,
+                      int64_t ldw, int N, const void* bias, void* C, int64_t ldc,
+                      cudaStream_t stream) {
+    cudaError_t err;
+    if (m->dtype == MHA_F32) {
+        err = mha::launch_gemm_f32(static_cast<const float*>(A), lda, static_cast<const float*>(W),
+                                   ldw, static_cast<const float*>(bias), static_cast<float*>(C),
+                                   ldc, M, N, K, stream);
+    } else {
+        int sms = 0;
+        const mha_status st = query_sms(&sms);
+        if (st != MHA_OK) return st;
+        err = mha::launch_gemm_bf16(A, lda, W, ldw, bias, C, ldc, M, N, K, sms, status_ptr(m),
+                                    stream);
+    }
+    return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+mha_status run_attention(const mha_s* m, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
+                         const void* K, int64_t ldk, const void* V, int64_t ldv, int causal,
+                         const int32_t* kv_lengths, void* O, int64_t ldo, cudaStream_t stream) {
+    cudaError_t err;
+    if (m->dtype == MHA_F32) {
+        err = mha::launch_attn_f32(static_cast<const float*>(Q), ldq, static_cast<const float*>(K),
+                                   ldk, static_cast<const float*>(V), ldv, static_cast<float*>(O),
+                                   ldo, B, m->h, T_q, T_kv, m->dk, m->dv, causal, kv_lengths,
+                                   status_ptr(m), stream);
+    } else {
+        err = mha::launch_attn_bf16(Q, ldq, K, ldk, V, ldv, O, ldo, B, m->h, T_q, T_kv, m->dk,
+                                    causal, kv_lengths, status_ptr(m), stream);
+    }
+    return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// Checks shared by the public attention and forward entry points.
+mha_status check_attention_shape(const mha_s* m, int B, int T_q, int T_kv, int causal) {
+    if (B < 0 || T_q < 0 || T_kv < 0) return MHA_ERR_INVALID_ARG;
+    if (causal && T_q != T_kv) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)B * m->h > INT32_MAX) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)B * T_q > INT32_MAX || (int64_t)B * T_kv > INT32_MAX) return MHA_ERR_INVALID_ARG;
+    if (m->dtype == MHA_F32) {
+        if (m->dk > 256 || m->dv > 256) return MHA_ERR_UNSUPPORTED;
+        if ((T_q + 15) / 16 > 65535) return MHA_ERR_UNSUPPORTED;
+    } else {
+        if (!bf16_shape_supported(m)) return MHA_ERR_UNSUPPORTED;
+        if ((T_q + 127) / 128 > 65535) return MHA_ERR_UNSUPPORTED;
+    }
+    return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype) {
+    if (out == nullptr) return MHA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (D <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)h * (2 * (int64_t)d_k + d_v) > INT32_MAX) return MHA_ERR_INVALID_ARG;
+    mha_s* m = static_cast<mha_s*>(calloc(1, sizeof(mha_s)));
+    if (m == nullptr) return MHA_ERR_INVALID_ARG;
+    m->D = D;
+    m->h = h;
+    m->dk = d_k;
+    m->dv = d_v;
+    m->dtype = dtype;
+    *out = m;
+    return MHA_OK;
+}
+
+void mha_destroy(mha_t handle) { free(handle); }
+
+size_t mha_workspace_size(mha_t handle, int B, int T_q, int T_kv) {
+    if (handle == nullptr || B < 0 || T_q < 0 || T_kv < 0) return 0;
+    return ws_layout(handle, B, T_q, T_kv).total;
+}
+
+mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    if (dev_ptr == nullptr) {
+        handle->ws = nullptr;
+        handle->ws_bytes = 0;
+        return MHA_OK;
+    }
+    if ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) != 0 || bytes < kStatusBytes)
+        return MHA_ERR_INVALID_ARG;
+    if (cudaMemset(dev_ptr, 0, kStatusBytes) != cudaSuccess) return MHA_ERR_CUDA;
+    handle->ws = dev_ptr;
+    handle->ws_bytes = bytes;
+    return MHA_OK;
+}
+
+mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
+                      int64_t ldw, int N, const void* bias, void* C, int64_t ldc, void* stream) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    if (M < 0 || K <= 0 || N <= 0) return MHA_ERR_INVALID_ARG;
+    if (M == 0) return MHA_OK;
+    if (A == nullptr || W == nullptr || C == nullptr) return MHA_ERR_INVALID_ARG;
+    if (lda < K || ldw < N || ldc < N) return MHA_ERR_INVALID_ARG;
+    if (handle->dtype == MHA_BF16) {
+        if ((K % 8) || (N % 8) || (lda % 8) || (ldw % 8) || (ldc % 8)) return MHA_ERR_INVALID_ARG;
+        if (!aligned16(A) || !aligned16(W) || !aligned16(C) || (bias && !aligned16(bias)))
+            return MHA_ERR_INVALID_ARG;
+    }
+    const size_t s = elem_bytes(handle->dtype);
+    if (overlaps(C, ((size_t)(M - 1) * ldc + N) * s, A, ((size_t)(M - 1) * lda + K) * s) ||
+        overlaps(C, ((size_t)(M - 1) * ldc + N) * s, W, ((size_t)(K - 1) * ldw + N) * s))
+        return MHA_ERR_INVALID_ARG;
+    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc,
+                      static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
+                         const void* K, int64_t ldk, const void* V, int64_t ldv, int causal,
+                         const int32_t* kv_lengths, void* O, int64_t ldo, void* stream) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    mha_status st = check_attention_shape(handle, B, T_q, T_kv, causal);
+    if (st != MHA_OK) return st;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    if (T_kv == 0) return MHA_ERR_INVALID_ARG;
+    if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return MHA_ERR_INVALID_ARG;
+    const int64_t hq = (int64_t)handle->h * handle->dk, hv = (int64_t)handle->h * handle->dv;
+    if (ldq < hq || ldk < hq || ldv < hv || ldo < hv) return MHA_ERR_INVALID_ARG;
+    if (handle->dtype == MHA_BF16) {
+        if ((ldq % 8) || (ldk % 8) || (ldv % 8) || (ldo % 8)) return MHA_ERR_INVALID_ARG;
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+            return MHA_ERR_INVALID_ARG;
+    }
+    return run_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths, O, ldo,
+                         static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                       const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                       int causal, const int32_t* kv_lengths, void* out, void* stream) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    const mha_s* m = handle;
+    const bool self = (X_kv == nullptr || X_kv == X_q);
+    if (self && T_kv != T_q) return MHA_ERR_INVALID_ARG;
+    mha_status st = check_attention_shape(m, B, T_q, T_kv, causal);
+    if (st != MHA_OK) return st;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    if (T_kv == 0) return MHA_ERR_INVALID_ARG;
+    if (X_q == nullptr || W_qkv == nullptr || W_o == nullptr || out == nullptr)
+        return MHA_ERR_INVALID_ARG;
+    if (m->dtype == MHA_BF16) {
+        if (!aligned16(X_q) || (X_kv && !aligned16(X_kv)) || !aligned16(W_qkv) ||
+            !aligned16(W_o) || !aligned16(out) || (b_qkv && !aligned16(b_qkv)) ||
+            (b_o && !aligned16(b_o)))
+            return MHA_ERR_INVALID_ARG;
+    }
+    const size_t s = elem_bytes(m->dtype);
+    const int64_t D = m->D;
+    const int64_t hq = (int64_t)m->h * m->dk, hv = (int64_t)m->h * m->dv;
+    const int64_t ncols = 2 * hq + hv;
+    const size_t out_bytes = (size_t)B * T_q * D * s;
+    if (overlaps(out, out_bytes, X_q, (size_t)B * T_q * D * s) ||
+        (!self && overlaps(out, out_bytes, X_kv, (size_t)B * T_kv * D * s)) ||
+        overlaps(out, out_bytes, W_qkv, (size_t)D * ncols * s) ||
+        overlaps(out, out_bytes, W_o, (size_t)hv * D * s))
+        return MHA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(m, B, T_q, T_kv);
+    if (m->ws == nullptr || m->ws_bytes < w.total) return MHA_ERR_WORKSPACE;
+
+    uint8_t* ws = static_cast<uint8_t*>(m->ws);
+    void* ocat = ws + w.o_off;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const uint8_t* wqkv = static_cast<const uint8_t*>(W_qkv);
+    const uint8_t* bqkv = static_cast<const uint8_t*>(b_qkv);
+
+    if (self) {
+        void* qkv = ws + w.q_off;
+        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)ncols, b_qkv, qkv, ncols, cs);
+        if (st != MHA_OK) return st;
+        const uint8_t* base = static_cast<const uint8_t*>(qkv);
+        st = run_attention(m, B, T_q, T_kv, base, ncols, base + hq * s, ncols, base + 2 * hq * s,
+                           ncols, causal, kv_lengths, ocat, hv, cs);
+        if (st != MHA_OK) return st;
+    } else {
+        void* q = ws + w.q_off;
+        void* kv = ws + w.kv_off;
+        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)hq, b_qkv, q, hq, cs);
+        if (st != MHA_OK) return st;
+        st = run_linear(m, X_kv, D, B * T_kv, (int)D, wqkv + hq * s, ncols, (int)(hq + hv),
+                        bqkv ? bqkv + hq * s : nullptr, kv, hq + hv, cs);
+        if (st != MHA_OK) return st;
+        const uint8_t* kvb = static_cast<const uint8_t*>(kv);
+        st = run_attention(m, B, T_q, T_kv, q, hq, kvb, hq + hv, kvb + hq * s, hq + hv, causal,
+                           kv_lengths, ocat, hv, cs);
+        if (st != MHA_OK) return st;
+    }
+    return run_linear(m, ocat, hv, B * T_q, (int)hv, W_o, D, (int)D, b_o, out, D, cs);
+}
+
+mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream) {
+    if (handle == nullptr || status_out == nullptr) return MHA_ERR_INVALID_ARG;
+    if (handle->ws == nullptr) return MHA_ERR_WORKSPACE;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, handle->ws, sizeof(v), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return MHA_ERR_CUDA;
+    if (cudaMemsetAsync(handle->ws, 0, sizeof(v), cs) != cudaSuccess) return MHA_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return MHA_ERR_CUDA;
+    *status_out = v;
+    return MHA_OK;
+}
+
+const char* mha_strerror(mha_status status) {
+    switch (status) {
+        case MHA_OK: return "ok";
+        case MHA_ERR_INVALID_ARG: return "invalid argument";
+        case MHA_ERR_UNSUPPORTED: return "shape or dtype not supported by this build";
+        case MHA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MHA_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case MHA_ERR_TIMEOUT: return "a device pipeline wait timed out";
+        case MHA_ERR_BAD_LENGTH: return "a key length is outside [1, T_kv]; its rows are NaN";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

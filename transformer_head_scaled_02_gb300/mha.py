@@ -1,0 +1,140 @@
+"""Torch-tensor front end of libmha.so.
+
+torch supplies device memory and the current CUDA stream; every step of the
+forward runs in the library's kernels.  This module only checks tensor
+properties, allocates the caller-side buffers (output and workspace) and
+passes raw pointers through the C ABI (see ``_lib``).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float32: _lib.MHA_F32, torch.bfloat16: _lib.MHA_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+class Mha:
+    """One multi-head attention layer shape: width D, h heads of d_k / d_v.
+
+    ``forward`` computes MultiHead(X_q, X_kv) = Concat(head_1..head_h) W_o + b_o
+    with head_i = softmax(Q_i K_i^T / sqrt(d_k) [+ mask]) V_i, the fused
+    [Q|K|V] projection X W_qkv + b_qkv feeding it (itwiki.kr "멀티 헤드 어텐션",
+    수식 and the tensor-shape table).
+    """
+
+    def __init__(self, D: int, h: int, d_k: int, d_v: Optional[int] = None,
+                 dtype: torch.dtype = torch.bfloat16, device=None):
+        if dtype not in _DTYPES:
+            raise TypeError(f"dtype must be one of {list(_DTYPES)}")
+        self.D, self.h, self.d_k = D, h, d_k
+        self.d_v = d_k if d_v is None else d_v
+        self.dtype = dtype
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.handle = _lib.mha_create(D, h, d_k, self.d_v, _DTYPES[dtype])
+        self._ws: Optional[torch.Tensor] = None
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            _lib.mha_destroy(h)
+            self.handle = None
+
+    # ------------------------------------------------------------ workspace
+    def workspace_size(self, B: int, T_q: int, T_kv: int) -> int:
+        return _lib.mha_workspace_size(self.handle, B, T_q, T_kv)
+
+    def ensure_workspace(self, B: int, T_q: int, T_kv: int) -> torch.Tensor:
+        need = self.workspace_size(B, T_q, T_kv)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            _lib.mha_set_workspace(self.handle, self._ws.data_ptr(), self._ws.numel())
+        return self._ws
+
+    def status(self) -> int:
+        """Read and clear the device status word (synchronises the current stream)."""
+        return _lib.mha_get_status(self.handle, _stream())
+
+    # ------------------------------------------------------------ checks
+    def _check(self, name, t, shape=None):
+        if t is None:
+            return
+        if not t.is_cuda or t.dtype != self.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {self.dtype} CUDA tensor")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+    # ------------------------------------------------------------ the layer
+    def forward(self, X_q: torch.Tensor, W_qkv: torch.Tensor, b_qkv: Optional[torch.Tensor],
+                W_o: torch.Tensor, b_o: Optional[torch.Tensor], X_kv: Optional[torch.Tensor] = None,
+                causal: bool = False, kv_lengths: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        B, T_q, D = X_q.shape
+        T_kv = T_q if X_kv is None else X_kv.shape[1]
+        ncols = 2 * self.h * self.d_k + self.h * self.d_v
+        self._check("X_q", X_q, (B, T_q, self.D))
+        self._check("X_kv", X_kv, None if X_kv is None else (B, T_kv, self.D))
+        self._check("W_qkv", W_qkv, (self.D, ncols))
+        self._check("b_qkv", b_qkv, None if b_qkv is None else (ncols,))
+        self._check("W_o", W_o, (self.h * self.d_v, self.D))
+        self._check("b_o", b_o, None if b_o is None else (self.D,))
+        if kv_lengths is not None and (kv_lengths.dtype != torch.int32 or not kv_lengths.is_cuda
+                                       or kv_lengths.numel() != B):
+            raise ValueError("kv_lengths must be a CUDA int32 tensor of length B")
+        if out is None:
+            out = torch.empty((B, T_q, self.D), dtype=self.dtype, device=X_q.device)
+        self._check("out", out, (B, T_q, self.D))
+        self.ensure_workspace(B, T_q, T_kv)
+        _lib.mha_forward(self.handle, _ptr(X_q), _ptr(X_kv), B, T_q, T_kv, _ptr(W_qkv),
+                         _ptr(b_qkv), _ptr(W_o), _ptr(b_o), causal, _ptr(kv_lengths),
+                         _ptr(out), _stream())
+        return out
+
+    __call__ = forward
+
+    # ------------------------------------------------------------ single steps
+    def linear(self, A: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """C = A W + bias for 2-D A (M, K), W (K, N) (row strides may exceed the width)."""
+        M, K = A.shape
+        N = W.shape[1]
+        if out is None:
+            out = torch.empty((M, N), dtype=self.dtype, device=A.device)
+        for name, t in (("A", A), ("W", W), ("out", out)):
+            if not t.is_cuda or t.dtype != self.dtype or t.stride(1) != 1:
+                raise ValueError(f"{name} must be a row-major {self.dtype} CUDA matrix")
+        self._check("bias", bias, None if bias is None else (N,))
+        _lib.mha_linear(self.handle, _ptr(A), A.stride(0), M, K, _ptr(W), W.stride(0), N,
+                        _ptr(bias), _ptr(out), out.stride(0), _stream())
+        return out
+
+    def attention(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal: bool = False,
+                  kv_lengths: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Attention of all heads over (B, T, width) views whose last dim is contiguous;
+        head i uses columns [i*d, (i+1)*d).  Returns Ocat (B, T_q, h*d_v)."""
+        B, T_q, _ = Q.shape
+        T_kv = K.shape[1]
+        for name, t in (("Q", Q), ("K", K), ("V", V)):
+            if not t.is_cuda or t.dtype != self.dtype or t.stride(2) != 1 \
+                    or t.stride(0) != t.shape[1] * t.stride(1):
+                raise ValueError(f"{name} must be a (B,T,*) {self.dtype} CUDA view with "
+                                 "contiguous rows and batches")
+        if out is None:
+            out = torch.empty((B, T_q, self.h * self.d_v), dtype=self.dtype, device=Q.device)
+        if kv_lengths is not None and (kv_lengths.dtype != torch.int32 or not kv_lengths.is_cuda):
+            raise ValueError("kv_lengths must be a CUDA int32 tensor")
+        _lib.mha_attention(self.handle, B, T_q, T_kv, _ptr(Q), Q.stride(1), _ptr(K), K.stride(1),
+                           _ptr(V), V.stride(1), causal, _ptr(kv_lengths), _ptr(out),
+                           out.stride(1), _stream())
+        return out

@@ -221,3 +221,11 @@ def hbm_bytes(w: Workload) -> float:
     y = w.B * w.T_q * w.D
     weights = w.D * w.w_cols + hv * w.D + w.w_cols + w.D
     return float(s * (x + 2 * qkv + 2 * ocat + y + weights))
+
+
+def random_tensor(shape, seed: int, dtype: str = "bf16", scale: float = 1.0) -> np.ndarray:
+    """A standalone N(0, scale^2) tensor (float32, bf16-rounded for "bf16"), for
+    tests of a single step (projection or attention) on given operands."""
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(scale)
+    return round_to_bf16(a) if dtype == "bf16" else a

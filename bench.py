@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Throughput of the multi-head attention forward on GB300, one JSON line.
+
+Metric: MHA forward TFLOP/s (bf16 causal, 1 x GB300) and % of the dense-BF16
+peak.  FLOPs per step follow itwiki.kr "멀티 헤드 어텐션", 매개변수와 계산량:
+8 T D^2 for the projections plus 4 T^2 D for scores and weighted sum, the
+latter halved under the causal mask, per batch element.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
+
+One step = one mha_forward of the whole workload (three kernels: QKV GEMM,
+fused attention, output GEMM) on inputs already resident in HBM; L2 is flushed
+(a 256 MiB write) before every timed step, outside the events that time it.
+Under torchrun each rank runs an independent replica (the layer does not
+shard: there is no exchange step), the timed region is bracketed by a barrier
+and a device synchronise, and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from transformer_head_scaled_02_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MHA forward TFLOP/s (bf16 causal, 1×GB300) and % of dense-BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "c3_bf16_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_source_hash(fname: str) -> str:
+    with open(os.path.join(ROOT, "transformer_head_scaled_02_gb300", "csrc", fname), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_sha256_16") != kernel_source_hash(src_file):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Polls SM clock, max clock, power and clock-event reasons through NVML
+    (read-only queries) every few ms on a background thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int = 0, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.dev = ctypes.c_void_p()
+            handle_found = False
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(device_index)
+                bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+                handle_found = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.dev)) == 0
+            except Exception:
+                handle_found = False
+            if not handle_found and self.nvml.nvmlDeviceGetHandleByIndex_v2(
+                    device_index, ctypes.byref(self.dev)) != 0:
+                return
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _poll(self):
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+            self.nvml.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(pw))
+            self._reasons_fn(self.dev, ctypes.byref(rs))
+            self.samples.append((time.time(), int(clk.value), pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "NVML not available"}
+        s = [x for x in self.samples if self.t0 <= x[0] <= self.t1] or self.samples
+        reasons = set()
+        for _, _, _, r in s:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[1] for x in s) if s else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons), "samples": len(s),
+                "power_w_max": max(x[2] for x in s) if s else None}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def to_device(a, dtype_name, torch):
+    import numpy as np
+    if a is None:
+        return None
+    if dtype_name == "bf16":
+        return torch.from_numpy(wl.bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: batch 0
+    and its first T' query rows (for causal self-attention the outputs of those rows
+    depend on nothing else), T' sized to take about budget_s on the host cores."""
+    import oracle
+    oracle.build()
+    x = wl.make_inputs(w)
+
+    def run(tp):
+        sub = dict(X_q=x["X_q"][:1, :tp], W_qkv=x["W_qkv"], b_qkv=x["b_qkv"], W_o=x["W_o"],
+                   b_o=x["b_o"])
+        t0 = time.perf_counter()
+        if w.cross:
+            L = None if x["kv_lengths"] is None else x["kv_lengths"][:1]
+            oracle.mha_forward(sub["X_q"], sub["W_qkv"], sub["b_qkv"], sub["W_o"], sub["b_o"], w.h,
+                               w.d_k, w.d_v, Xkv=x["X_kv"][:1], causal=w.causal, kv_lengths=L)
+        else:
+            oracle.mha_forward(sub["X_q"], sub["W_qkv"], sub["b_qkv"], sub["W_o"], sub["b_o"], w.h,
+                               w.d_k, w.d_v, causal=w.causal)
+        return time.perf_counter() - t0
+
+    tp = min(w.T_q, 64)
+    dt = run(tp)
+    while tp < w.T_q and dt < budget_s / 4:
+        tp = min(w.T_q, tp * 2)
+        dt = run(tp)
+    sw = wl.custom("sample", B=1, T_q=tp, T_kv=w.T_kv if w.cross else tp, D=w.D, h=w.h, d_k=w.d_k,
+                   d_v=w.d_v, dtype=w.dtype, causal=w.causal, cross=w.cross)
+    f = wl.flops(sw)["total"]
+    return {"value": f / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"batch 0, first {tp} of {w.T_q} query rows of {w.name} "
+                      f"({'all ' + str(w.T_kv) + ' keys' if w.cross else 'causal prefix'}), fp64, "
+                      f"{dt:.2f} s"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__ as g
+    g.build_library()
+    from transformer_head_scaled_02_gb300 import Mha
+
+    w = wl.WORKLOADS[args.workload]
+    x = wl.make_inputs(w)
+    d = {k: to_device(v, w.dtype, torch) for k, v in x.items() if k != "kv_lengths"}
+    kvl = None if x["kv_lengths"] is None else torch.from_numpy(x["kv_lengths"]).cuda()
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    layer = Mha(w.D, w.h, w.d_k, w.d_v, dtype=tdt)
+    out = torch.empty((w.B, w.T_q, w.D), dtype=tdt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = 4 if w.cross else 3
+
+    def forward():
+        layer.forward(d["X_q"], d["W_qkv"], d["b_qkv"], d["W_o"], d["b_o"], X_kv=d["X_kv"],
+                      causal=w.causal, kv_lengths=kvl, out=out)
+
+    for _ in range(args.warmup):
+        forward()
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError("device status not clean after warm-up")
+
+    # ---------------- timed region: K steps, each timed by events, L2 flushed between
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.05)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record()
+        forward()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    ms_per_step = total_ms / K
+    if layer.status() != 0:
+        raise RuntimeError("device status reports an error after the timed region")
+
+    fl = wl.flops(w, x["kv_lengths"])
+    step_flops = fl["total"]
+    value = world * step_flops / (ms_per_step / 1e3) / 1e12
+
+    # ---------------- per-kernel durations: the same three launches, events between them
+    sf = wl.step_flops(w)
+    names = ["qkv_proj", "attention", "out_proj"]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    Wqkv, bqkv = d["W_qkv"], d["b_qkv"]
+    hq, hv = w.h * w.d_k, w.h * w.d_v
+    ncols = 2 * hq + hv
+    qkv = torch.empty((w.B, w.T_q, ncols), dtype=tdt, device=dev)
+    ocat = torch.empty((w.B, w.T_q, hv), dtype=tdt, device=dev)
+    per_kernel = None
+    if not w.cross:
+        X2 = d["X_q"].view(-1, w.D)
+        for k in range(K):
+            flush.zero_()
+            e = kev[k]
+            e[0].record()
+            layer.linear(X2, Wqkv, bqkv, out=qkv.view(-1, ncols))
+            e[1].record()
+            layer.attention(qkv[..., :hq], qkv[..., hq:2 * hq], qkv[..., 2 * hq:], causal=w.causal,
+                            out=ocat)
+            e[2].record()
+            layer.linear(ocat.view(-1, hv), d["W_o"], d["b_o"], out=out.view(-1, w.D))
+            e[3].record()
+        torch.cuda.synchronize()
+        per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
+                      for i, n in enumerate(names)}
+
+    # ---------------- end to end through the public API, host buffers in and out
+    xh = d["X_q"].cpu().pin_memory()
+    xkvh = None if d["X_kv"] is None else d["X_kv"].cpu().pin_memory()
+    yh = torch.empty(out.shape, dtype=tdt).pin_memory()
+    Ke = min(K, 50)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ke)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(Ke):
+        flush.zero_()
+        eev[k][0].record()
+        d["X_q"].copy_(xh, non_blocking=True)
+        if xkvh is not None:
+            d["X_kv"].copy_(xkvh, non_blocking=True)
+        forward()
+        yh.copy_(out, non_blocking=True)
+        eev[k][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), world, dev) / Ke
+    h2d = xh.numel() * xh.element_size() + (0 if xkvh is None else xkvh.numel() * xkvh.element_size())
+    d2h = yh.numel() * yh.element_size()
+
+    pk, pk_src = peaks()
+    roofline = None
+    if per_kernel:
+        top = max(per_kernel, key=per_kernel.get)
+        src = "attn_bf16.cu" if top == "attention" else "gemm_bf16.cu"
+        if w.dtype == "f32":
+            src = "simt_f32.cu"
+        ach = sf[top] / (per_kernel[top] / 1e3) / 1e12
+        peak = pk["bf16_tflops"]
+        roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                    "traffic": recorded_traffic(top, w.name, src),
+                    "peak_source": f"{pk_src} bf16 dense (burst)",
+                    "per_kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
+                    "per_kernel_frac_of_peak": {k: round(sf[k] / (v / 1e3) / 1e12 / peak, 4)
+                                                for k, v in per_kernel.items()}}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "T_q": w.T_q, "T_kv": w.T_kv, "D": w.D,
+                   "h": w.h, "d_k": w.d_k, "d_v": w.d_v, "causal": w.causal, "cross": w.cross,
+                   "flops_per_step": step_flops, "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+                   "peak_tflops": pk["bf16_tflops"], "peak_source": pk_src,
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4),
+                "note": "mha_forward via the public API with pinned host X in and Y out; "
+                        "weights resident"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": sampler.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_baseline_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, each step a bounded sample of the workload
+    (batch 0, a prefix of T' query rows), T' sized so the whole run takes about
+    --reference-seconds."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    x = wl.make_inputs(w)
+
+    def step(tp):
+        t0 = time.perf_counter()
+        if w.cross:
+            L = None if x["kv_lengths"] is None else x["kv_lengths"][:1]
+            oracle.mha_forward(x["X_q"][:1, :tp], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h,
+                               w.d_k, w.d_v, Xkv=x["X_kv"][:1], causal=w.causal, kv_lengths=L)
+        else:
+            oracle.mha_forward(x["X_q"][:1, :tp], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h,
+                               w.d_k, w.d_v, causal=w.causal)
+        return time.perf_counter() - t0
+
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
+    tp = 16
+    dt = step(tp)
+    while tp < w.T_q and dt * 2 < per_step:
+        tp = min(w.T_q, tp * 2)
+        dt = step(tp)
+    for _ in range(args.warmup):
+        step(tp)
+    times = [step(tp) for _ in range(args.steps)]
+    sw = wl.custom("sample", B=1, T_q=tp, T_kv=w.T_kv if w.cross else tp, D=w.D, h=w.h, d_k=w.d_k,
+                   d_v=w.d_v, dtype=w.dtype, causal=w.causal, cross=w.cross)
+    f = wl.flops(sw)["total"]
+    ms = 1e3 * sum(times) / len(times)
+    value = f / (ms / 1e3) / 1e12
+    sample = (f"batch 0, first {tp} of {w.T_q} query rows of {w.name} per step, fp64 oracle "
+              f"on {oracle.max_threads()} host threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample_rows": tp},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

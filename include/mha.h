@@ -160,6 +160,42 @@ mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream);
 /* mha_strerror -- static description of a status code. */
 const char* mha_strerror(mha_status status);
 
+/* Size of the library-owned scratch array behind mha_forward_static_workspace: 32 MiB. */
+#define MHA_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * mha_forward_static_workspace -- mha_forward for callers that may not allocate device
+ * memory.  The pages have no counterpart to this call: they define the operation, not how
+ * its scratch memory is provided.
+ *
+ * Who needs it: code that cannot call cudaMalloc (or ask anyone to) -- for example a library
+ * embedded in a host framework that owns every device allocation through its own pool and
+ * hands plugins no scratch buffer, or a latency-critical serving loop where cudaMalloc's
+ * implicit device-wide synchronisation is not acceptable.  Such a caller still owns and
+ * passes every input and the output; only the scratch (status word, projected Q/K/V, Ocat)
+ * comes from a file-scope __device__ array of MHA_STATIC_WORKSPACE_BYTES inside this library.
+ * Every GPU that loads the library holds that array until the process exits.
+ *
+ *  - Arguments, layouts and result are those of mha_forward.  The handle's own workspace
+ *    (mha_set_workspace) is neither used nor modified.
+ *  - Returns MHA_ERR_WORKSPACE, before any CUDA call, when mha_workspace_size(B, T_q, T_kv)
+ *    exceeds MHA_STATIC_WORKSPACE_BYTES.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *    with that device current) and remembers it; make that first call before any stream
+ *    capture.
+ *  - All calls share the one array, which keeps the previous call's contents: calls that
+ *    overlap on the GPU (other streams or host threads on the same device) race on it and
+ *    must be serialised by the caller.
+ *  - Each call zeroes the status word first (cudaMemsetAsync on `stream`).  An L_b outside
+ *    [1, T_kv] still gives NaN rows, but the status word cannot be read back: mha_get_status
+ *    reads the handle's own workspace.
+ */
+mha_status mha_forward_static_workspace(mha_t handle, const void* X_q, const void* X_kv, int B,
+                                        int T_q, int T_kv, const void* W_qkv, const void* b_qkv,
+                                        const void* W_o, const void* b_o, int causal,
+                                        const int32_t* kv_lengths, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

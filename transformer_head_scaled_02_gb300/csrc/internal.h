@@ -4,7 +4,18 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
+
+#include "../../include/mha.h"
+
+// The opaque handle of include/mha.h: the layer configuration and the caller's workspace.
+struct mha_s {
+    int D, h, dk, dv;
+    mha_dtype dtype;
+    void* ws;
+    size_t ws_bytes;
+};
 
 namespace mha {
 

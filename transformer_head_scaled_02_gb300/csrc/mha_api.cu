@@ -19,13 +19,6 @@
 #include "../../include/mha.h"
 #include "internal.h"
 
-struct mha_s {
-    int D, h, dk, dv;
-    mha_dtype dtype;
-    void* ws;
-    size_t ws_bytes;
-};
-
 namespace mha {
 
 // ------------------------------------------------------------------ tensor maps

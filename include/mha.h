@@ -67,8 +67,9 @@ typedef enum {
  *   W_i^V in R^{d_model x d_v}, W^O in R^{h d_v x d_model}).
  * Any positive D, h, d_k, d_v is accepted here; a dtype/shape pair without a
  * kernel is reported by the compute calls as MHA_ERR_UNSUPPORTED.
- * Returns MHA_ERR_INVALID_ARG for out == NULL or a non-positive size, and
- * MHA_ERR_CUDA if no CUDA device can be queried.  Host memory only.
+ * Returns MHA_ERR_INVALID_ARG for out == NULL, a non-positive size or an
+ * unknown dtype.  Host memory only; makes no CUDA call, so it also works on a
+ * machine without a GPU.
  */
 mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype);
 
@@ -112,9 +113,10 @@ mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes);
  *   out    (B, T_q, D)
  * Needs a workspace of mha_workspace_size(B, T_q, T_kv) bytes.  Launches
  * three kernels (self) or four (cross) on `stream`.
- * bf16 requires d_k == d_v in {64, 128}, D and h*d_k multiples of 64 and
- * 16-byte aligned pointers (else MHA_ERR_UNSUPPORTED / MHA_ERR_INVALID_ARG);
- * fp32 accepts any shape with d_k, d_v <= 256.
+ * bf16 requires d_k == d_v in {64, 128} and D a multiple of 8 (else
+ * MHA_ERR_UNSUPPORTED) and 16-byte aligned pointers (else MHA_ERR_INVALID_ARG);
+ * fp32 accepts any shape with d_k, d_v <= 256.  B == 0 or T_q == 0 is a no-op;
+ * T_kv == 0 with T_q > 0 is MHA_ERR_INVALID_ARG.
  */
 mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
                        const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,

@@ -7,27 +7,42 @@
 // iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", sections 9-10 (mask as -inf,
 // row softmax) and 19 (cross-attention).
 //
-// One CTA computes one (batch, head, 128-row query tile).  The softmax is the online form:
-// a running row maximum m and sum l, with O rescaled when m grows, so the result equals the
-// row softmax after the final division by l.  Everything stays in base 2: p = 2^(s*c - m)
-// with c = log2(e)/sqrt(d) folded into one FFMA per score.
+// One CTA computes two 128-row query tiles (Q0, Q1: 256 consecutive rows) of one
+// (batch, head); both tiles share every K/V tile the TMA brings in, which halves the
+// L2->SMEM traffic per FLOP.  The softmax is the online form: a running row maximum m and
+// sum l, with O rescaled when m grows, so the result equals the row softmax after the final
+// division by l.  Everything stays in base 2: p = 2^(s*c - m) with c = log2(e)/sqrt(d) folded
+// into one FMA per score.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA loads: the Q tile once, then K and V tiles (128 keys) into a ring;
-//   warp 1      TMEM owner and single-thread MMA issuer:
-//                 S_j = Q K_j^T   (M=128, N=128, K=d; double-buffered S in TMEM)
-//                 O  += P_j V_j   (M=128, N=d, K=128; O accumulates in TMEM)
-//               S_{j+1} is issued before waiting for P_j, so the tensor core computes the
-//               next scores while the softmax warps work on the current ones;
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): read S_j, mask, row
-//               max, exponentials, row sum, write P_j (bf16, swizzled K-major) to shared
-//               memory, rescale O in TMEM when needed; at the end O/l is rounded to bf16
-//               and written by TMA straight into column block i*d of the (B,T,h*d) output.
-// The rescale is lazy: the reference maximum only moves when a tile's maximum exceeds it by
-// more than 8 (a factor 256 in base 2), so most tiles skip the O read-modify-write; the
-// final O/l is the same because numerator and denominator share the reference.
-// Causal: query tile qt needs key tiles 0..qt only; the grid runs the heaviest tiles first.
-// Key padding: key tiles stop at ceil(L_b/128); the last one is masked in registers.
+// Tensor memory (512 columns, one CTA per SM):
+//   S_t  [128 t, 128 t + 128)      scores of query tile t, fp32; once read, the same columns
+//                                  receive P_t as packed bf16 pairs (64 columns)
+//   O_t  [256 + d t, 256 + d t + d) output accumulator of tile t, fp32
+//   Q_t  [384 + 32 t, ...)          (d = 64 only) the query tile itself, packed bf16
+// Both GEMMs read their A operand from TMEM when it lives there (P always; Q for d = 64), so
+// shared memory only feeds the K and V operands.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a ring of stages;
+//   warp 1      TMEM owner and single-thread MMA issuer.  Per key tile j:
+//                 O_0 += P_0 V_j ; S_0 = Q_0 K_{j+1}^T ; O_1 += P_1 V_j ; S_1 = Q_1 K_{j+1}^T
+//               (tcgen05 MMAs of one thread execute in issue order, so S_t may overwrite the
+//               P_t columns right after the MMA that reads them);
+//   warps 2-3   idle;
+//   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1 -- one row per thread (TMEM
+//               lane = row): read S, mask, row max, exponentials, row sum, P -> TMEM, lazy
+//               O rescale; while one group works, the tensor core runs the other tile's MMAs.
+//               At the end O/l is rounded to bf16 and stored by TMA straight into column
+//               block (head * d) of the (B, T, h*d) Concat output.
+// The rescale is lazy: the reference maximum moves only when a tile's maximum exceeds it by
+// more than 8 (a factor 256 in base 2); numerator and denominator share the reference, so the
+// final O/l is unchanged.
+// exp2: three quarters of the exponentials go to the MUFU unit (ex2.approx); one quarter is
+// computed on the FMA pipe -- x = n + f with n = round(x) by the 1.5*2^23 magic-number add,
+// 2^f by a degree-3 polynomial whose coefficients are the minimax (relative error, Remez
+// exchange) fit of 2^f on [-1/2, 1/2], max relative error 7.5e-5, and 2^n added into the
+// exponent field.  P is rounded to bf16 (relative step 2^-9) right after, so the polynomial
+// error is invisible.  Tiles with masked entries use MUFU only, so masked weights are exactly 0.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -36,24 +51,38 @@ namespace {
 
 template <int HD>
 struct AttnCfg {
-    static constexpr int BM = 128;                 // query rows per CTA
-    static constexpr int BN = 128;                 // keys per tile
-    static constexpr int CH = HD / 64;             // 64-column chunks per head
-    static constexpr int CHUNK = 128 * 128;        // 128 rows x 64 bf16 (128 B) = 16 KB
-    static constexpr int Q_BYTES = CH * CHUNK;
-    static constexpr int KV_BYTES = CH * CHUNK;    // one K (or V) tile
-    static constexpr int P_BYTES = 2 * CHUNK;      // 128 rows x 128 keys
-    static constexpr int STAGES = HD == 64 ? 4 : 2;
+    static constexpr int BM = 128;                  // rows per query tile
+    static constexpr int NQ = 2;                    // query tiles per CTA
+    static constexpr int BN = 128;                  // keys per tile
+    static constexpr int CH = HD / 64;              // 64-column chunks per head
+    static constexpr int CHUNK = 128 * 128;         // 128 rows x 64 bf16 (128 B) = 16 KB
+    static constexpr int Q_BYTES = CH * CHUNK;      // one query tile
+    static constexpr int KV_BYTES = CH * CHUNK;     // one K (or V) tile
+    static constexpr int STAGES = HD == 64 ? 5 : 2;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = Q_BYTES + 2 * STAGES * KV_BYTES + P_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + BAR_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 256;         // S buffers at columns 0 and 128
+    static constexpr bool Q_IN_TMEM = HD == 64;
+    __host__ __device__ static constexpr uint32_t S_COL(int t) { return (uint32_t)(128 * t); }
+    __host__ __device__ static constexpr uint32_t O_COL(int t) { return (uint32_t)(256 + HD * t); }
+    __host__ __device__ static constexpr uint32_t Q_COL(int t) { return (uint32_t)(384 + 32 * t); }
 };
 
 static_assert(AttnCfg<64>::SMEM <= 232448, "smem budget d=64");
 static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 
-constexpr int A_THREADS = 192;
+constexpr int A_THREADS = 384;
+
+// Which exponential pairs (of the 64 per row and key tile) go to the FMA-pipe polynomial;
+// the rest use MUFU.  d = 64 has half the MMA work per exponential of d = 128, so it moves
+// more of them off the MUFU unit.
+#define POLY_SEL(k) (HD == 64 ? ((k) % 8 >= 5) : ((k) % 4 == 3))
+
+// Minimax coefficients of 2^f on [-1/2, 1/2] (relative error), degree 3, lowest first.
+constexpr float kExp2C0 = 0.99992806f;
+constexpr float kExp2C1 = 0.69326097f;
+constexpr float kExp2C2 = 0.24261113f;
+constexpr float kExp2C3 = 0.05517167f;
 
 __device__ __forceinline__ void drain_wait_a(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -62,12 +91,74 @@ __device__ __forceinline__ void drain_wait_a(uint32_t bar, uint32_t parity) {
     }
 }
 
+// D(tmem) (+)= A(tmem) * B(smem): the A operand (M=128 rows, packed bf16 pairs along K)
+// comes from tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 2^x for a pair of finite x >= -126 on the FMA pipe (see the top of the file).
+__device__ __forceinline__ void exp2_poly_pair(uint64_t x, float& y0, float& y1) {
+    const uint64_t magic = pack2(12582912.0f, 12582912.0f);
+    const uint64_t t = add2(x, magic);   // round-to-nearest integer in the low mantissa bits
+    const uint64_t n = sub2(t, magic);
+    const uint64_t f = sub2(x, n);       // f in [-1/2, 1/2]
+    uint64_t p = fma2(pack2(kExp2C3, kExp2C3), f, pack2(kExp2C2, kExp2C2));
+    p = fma2(p, f, pack2(kExp2C1, kExp2C1));
+    p = fma2(p, f, pack2(kExp2C0, kExp2C0));
+    float p0, p1, t0, t1;
+    unpack2(p, p0, p1);
+    unpack2(t, t0, t1);
+    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
 template <int HD>
 __global__ void __launch_bounds__(A_THREADS, 1)
     attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
-                        const __grid_constant__ CUtensorMap tmO, int h, int T_kv, int causal,
+                        const __grid_constant__ CUtensorMap tmO, int h, int T_q, int T_kv, int causal,
                         const int32_t* __restrict__ kv_lengths, float scale_log2, int* status) {
     using C = AttnCfg<HD>;
     constexpr int S = C::STAGES;
@@ -76,22 +167,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
 
-    const uint32_t sQ = base;
-    const uint32_t sK = sQ + C::Q_BYTES;
+    const uint32_t sQ = base;  // Q0 then Q1; each later reused as that tile's output staging
+    const uint32_t sK = sQ + C::NQ * C::Q_BYTES;
     const uint32_t sV = sK + S * C::KV_BYTES;
-    const uint32_t sP = sV + S * C::KV_BYTES;
-    const uint32_t sBar = sP + C::P_BYTES;
-    // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], s_free[2], p_full,
-    //           pv_done, mma_drain
+    const uint32_t sBar = sV + S * C::KV_BYTES;
+    // barriers: q_full, q_tmem, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
+    //           o_done[2], mma_drain
     const uint32_t bar_q = sBar;
-    const uint32_t bar_kfull = sBar + 8u;
+    const uint32_t bar_qtmem = sBar + 8u;
+    const uint32_t bar_kfull = sBar + 16u;
     const uint32_t bar_vfull = bar_kfull + 8u * S;
     const uint32_t bar_kvempty = bar_vfull + 8u * S;
     const uint32_t bar_sfull = bar_kvempty + 8u * S;
-    const uint32_t bar_sfree = bar_sfull + 16u;
-    const uint32_t bar_pfull = bar_sfree + 16u;
-    const uint32_t bar_pvdone = bar_pfull + 8u;
-    const uint32_t bar_drain = bar_pvdone + 8u;
+    const uint32_t bar_pfull = bar_sfull + 16u;
+    const uint32_t bar_odone = bar_pfull + 16u;
+    const uint32_t bar_drain = bar_odone + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -100,28 +190,37 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int bh = blockIdx.x;
     const int b = bh / h;
     const int head = bh - b * h;
-    const int qt = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
-    const int q0 = qt * C::BM;
+    const int qb = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+    const int q0 = qb * (C::NQ * C::BM);
 
     const int L = kv_lengths != nullptr ? kv_lengths[b] : T_kv;
     const bool bad = L < 1 || L > T_kv;
-    int kv_hi = L;
-    if (causal && kv_hi > q0 + C::BM) kv_hi = q0 + C::BM;
-    const int n_tiles = bad ? 0 : (kv_hi + C::BN - 1) / C::BN;
+    const int nL = (L + C::BN - 1) / C::BN;
+    int n_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        int n = nL;
+        if (causal) {
+            const int nc = (q0 + C::BM * t + C::BM + C::BN - 1) / C::BN;  // key tiles up to the diagonal
+            n = n < nc ? n : nc;
+        }
+        n_t[t] = bad ? 0 : n;
+    }
+    const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
+        mbar_init(bar_qtmem, 256);
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_kfull + 8u * s, 1);
             mbar_init(bar_vfull + 8u * s, 1);
             mbar_init(bar_kvempty + 8u * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_sfull + 8u * s, 1);
-            mbar_init(bar_sfree + 8u * s, 128);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar_sfull + 8u * t, 1);
+            mbar_init(bar_pfull + 8u * t, 128);
+            mbar_init(bar_odone + 8u * t, 1);
         }
-        mbar_init(bar_pfull, 128);
-        mbar_init(bar_pvdone, 1);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -137,16 +236,19 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_max > 0) {
             // ---------------- TMA loads
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+            mbar_arrive_expect_tx(bar_q, C::NQ * C::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::CH; ++c)
-                tma_load_3d(sQ + c * C::CHUNK, &tmQ, head * HD + c * 64, q0, b, bar_q);
+            for (int t = 0; t < C::NQ; ++t)
+#pragma unroll
+                for (int c = 0; c < C::CH; ++c)
+                    tma_load_3d(sQ + t * C::Q_BYTES + c * C::CHUNK, &tmQ, head * HD + c * 64,
+                                q0 + t * C::BM, b, bar_q);
             int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
+            for (int j = 0; j < n_max; ++j) {
                 const int st = j % S;
                 const uint32_t ph = (uint32_t)(j / S) & 1u;
                 if (!mbar_wait(bar_kvempty + 8u * st, ph ^ 1u, abort_flag, status)) break;
@@ -173,160 +275,251 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_max > 0) {
             // ---------------- MMA issuer
+            // Descriptors are built once; per MMA only the start-address field changes, by
+            // adding the (16-byte granular) offset of the K step to the stage's descriptor.
             const uint32_t idesc_s = idesc_bf16_f32(128, C::BN, false, false);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
+            const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sV, C::CHUNK, 1024);
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             bool ok = mbar_wait(bar_q, 0, abort_flag, status);
-            for (int j = 0; j <= n_tiles && ok; ++j) {
-                if (j < n_tiles) {
-                    const int st = j % S;
-                    const uint32_t ph = (uint32_t)(j / S) & 1u;
-                    const int sb = j & 1;
-                    const uint32_t sph = (uint32_t)(j >> 1) & 1u;
-                    if (!mbar_wait(bar_kfull + 8u * st, ph, abort_flag, status)) break;
-                    if (!mbar_wait(bar_sfree + 8u * sb, sph ^ 1u, abort_flag, status)) break;
-                    tc_fence_after();
-                    const uint32_t kbase = sK + st * C::KV_BYTES;
+            if (C::Q_IN_TMEM) ok = ok && mbar_wait(bar_qtmem, 0, abort_flag, status);
+            int k_ready = -1;  // highest key tile whose K has been waited for
+            if (ok) {
+                ok = mbar_wait(bar_kfull, 0, abort_flag, status);
+                k_ready = 0;
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (n_t[t] == 0) continue;
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off = (uint32_t)((kk >> 2) * C::CHUNK + (kk & 3) * 32);
-                        mma_bf16_ss(tmem_base + (uint32_t)(sb * 128), sdesc_sw128(sQ + off, 16, 1024),
-                                    sdesc_sw128(kbase + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                        const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
+                        if (C::Q_IN_TMEM)
+                            mma_bf16_ts(tmem_base + C::S_COL(t), tmem_base + C::Q_COL(t) + kk * 8,
+                                        kdesc0 + off16, idesc_s, kk > 0 ? 1u : 0u);
+                        else
+                            mma_bf16_ss(tmem_base + C::S_COL(t),
+                                        qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4) + off16,
+                                        kdesc0 + off16, idesc_s, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bar_sfull + 8u * sb);
+                    tc_commit(bar_sfull + 8u * t);
                 }
-                if (j > 0) {
-                    const int i = j - 1;
-                    const int st = i % S;
-                    const uint32_t ph = (uint32_t)(i / S) & 1u;
-                    if (!mbar_wait(bar_pfull, (uint32_t)i & 1u, abort_flag, status)) break;
-                    if (!mbar_wait(bar_vfull + 8u * st, ph, abort_flag, status)) break;
-                    tc_fence_after();
-                    const uint32_t vbase = sV + st * C::KV_BYTES;
+            }
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int st = j % S;
+                if (!mbar_wait(bar_vfull + 8u * st, (uint32_t)(j / S) & 1u, abort_flag, status)) break;
+                const uint64_t vdesc = vdesc0 + (uint64_t)((st * C::KV_BYTES) >> 4);
+                const int jn = j + 1;
+                const uint64_t kdesc = kdesc0 + (uint64_t)(((jn % S) * C::KV_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; ++kk) {
-                        const uint32_t poff = (uint32_t)((kk >> 2) * C::CHUNK + (kk & 3) * 32);
-                        mma_bf16_ss(tmem_base + C::O_COL, sdesc_sw128(sP + poff, 16, 1024),
-                                    sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024), idesc_o,
-                                    (i > 0 || kk > 0) ? 1u : 0u);
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= n_t[t]) continue;
+                    if (!mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
                     }
-                    tc_commit(bar_kvempty + 8u * st);
-                    tc_commit(bar_pvdone);
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk)
+                        mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::S_COL(t) + kk * 8,
+                                    vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    if (jn < n_t[t]) {
+                        if (jn > k_ready) {
+                            if (!mbar_wait(bar_kfull + 8u * (jn % S), (uint32_t)(jn / S) & 1u,
+                                           abort_flag, status)) {
+                                ok = false;
+                                break;
+                            }
+                            k_ready = jn;
+                            tc_fence_after();
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            const uint32_t off16 =
+                                (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
+                            if (C::Q_IN_TMEM)
+                                mma_bf16_ts(tmem_base + C::S_COL(t),
+                                            tmem_base + C::Q_COL(t) + kk * 8, kdesc + off16, idesc_s,
+                                            kk > 0 ? 1u : 0u);
+                            else
+                                mma_bf16_ss(tmem_base + C::S_COL(t),
+                                            qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4) + off16,
+                                            kdesc + off16, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar_sfull + 8u * t);
+                    } else {
+                        tc_commit(bar_odone + 8u * t);
+                    }
                 }
+                if (!ok) break;
+                tc_commit(bar_kvempty + 8u * st);
             }
             tc_commit(bar_drain);
             drain_wait_a(bar_drain, 0);
         }
-    } else {
-        // ---------------- softmax: warps 2..5, thread = query row
+    } else if (warp >= 4) {
+        // ---------------- softmax: warps 4-7 tile 0, warps 8-11 tile 1; thread = query row
+        const int t = (warp - 4) >> 2;
         const int q = warp & 3;
         const int r = q * 32 + lane;
-        const int t = q0 + r;
+        const int qrow0 = q0 + t * C::BM;      // first row of this query tile
+        const int row = qrow0 + r;             // this thread's query row
+        const int n = n_t[t];
         const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
-        const uint32_t srow_sw = (uint32_t)(r & 7);
-        if (n_tiles == 0) {
+        const uint32_t sw = (uint32_t)(r & 7);
+        const uint32_t sQt = sQ + t * C::Q_BYTES;
+        const uint32_t bar_s = bar_sfull + 8u * t, bar_p = bar_pfull + 8u * t;
+        bool ok = true;
+
+        if (C::Q_IN_TMEM && n_max > 0) {
+            // Q row -> TMEM (packed bf16 pairs, 32 columns) for the TMEM-operand score MMA
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag, status));
+            if (ok) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        gbase + (sQt - base) + r * 128 + ((u ^ sw) << 4));
+                    qv[4 * u] = v.x;
+                    qv[4 * u + 1] = v.y;
+                    qv[4 * u + 2] = v.z;
+                    qv[4 * u + 3] = v.w;
+                }
+                tmem_st32(trow + C::Q_COL(t), qv);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(bar_qtmem);
+        }
+
+        if (n == 0) {
             // no valid key: the softmax is undefined, the rows are NaN
 #pragma unroll
             for (int c = 0; c < C::CH; ++c)
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    st_shared_v4(sQ + c * C::CHUNK + r * 128 + ((u ^ srow_sw) << 4), 0x7FC07FC0u,
+                    st_shared_v4(sQt + c * C::CHUNK + r * 128 + ((u ^ sw) << 4), 0x7FC07FC0u,
                                  0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
         } else {
             float m = -INFINITY;  // reference maximum, already scaled to base 2
             float l = 0.f;
-            bool ok = true;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int sb = j & 1;
+            const uint64_t c2 = pack2(scale_log2, scale_log2);
+            for (int j = 0; j < n && ok; ++j) {
                 // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull + 8u * sb, (uint32_t)(j >> 1) & 1u,
-                                                       abort_flag, status))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)j & 1u, abort_flag, status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(trow + (uint32_t)(sb * 128 + c * 32), sr[c]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar_sfree + 8u * sb);
-
                 float x[128];
+                {
+                    uint32_t sr[4][32];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(trow + C::S_COL(t) + c * 32, sr[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                }
                 const int kv0 = j * C::BN;
-                if (kv0 + C::BN > L || (causal && kv0 + C::BN - 1 > q0)) {
-                    const int lim = causal ? min(L, t + 1) : L;  // keys [0, lim) are visible
+                const bool masked = kv0 + C::BN > L || (causal && kv0 + C::BN - 1 > qrow0);
+                if (masked) {
+                    const int lim = causal ? min(L, row + 1) : L;  // keys [0, lim) are visible
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (kv0 + c >= lim) x[c] = -INFINITY;
                 }
-                float mx = x[0];
+                // row maximum: 8 independent chains of 3-input max
+                float mk[8];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+                for (int k = 0; k < 8; ++k) mk[k] = x[k];
+#pragma unroll
+                for (int c = 8; c < 128; c += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + k], x[c + 8 + k]);
+                const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                                       fmaxf(mk[6], mk[7]));
                 const float m_tile = mx * scale_log2;
                 float m_new = m;
                 if (m_tile > m + 8.0f) m_new = m_tile;
                 const bool rescale = (m_new != m) && j > 0;
                 const float alpha = ex2_approx(m - m_new);
                 const float neg = m_new == -INFINITY ? 0.f : -m_new;
-                float rowsum = 0.f;
+                const uint64_t neg2 = pack2(neg, neg);
+
+                // exponentials, row sum (4 packed partial sums), P as packed bf16
+                uint32_t pk[64];
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                if (masked) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    x[c] = ex2_approx(fmaf(x[c], scale_log2, neg));
-                    rowsum += x[c];
-                }
-                if (j > 0) {
-                    // P_{j-1} V_{j-1} finished: O is stable and the P buffer is free
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone, (uint32_t)(j - 1) & 1u,
-                                                           abort_flag, status))) {
-                        ok = false;
-                        break;
+                    for (int k = 0; k < 64; ++k) {
+                        float a0, a1;
+                        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
+                        const float y0 = ex2_approx(a0), y1 = ex2_approx(a1);
+                        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
+                        pk[k] = pack_bf16x2(y0, y1);
                     }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, rescale)) {
-                        const float a = rescale ? alpha : 1.f;
+                } else {
 #pragma unroll
-                        for (int cc = 0; cc < HD / 32; ++cc) {
-                            uint32_t o[32];
-                            tmem_ld32(trow + C::O_COL + cc * 32, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                            tmem_st32(trow + C::O_COL + cc * 32, o);
+                    for (int k = 0; k < 64; ++k) {
+                        float a0, a1, y0, y1;
+                        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
+                        if (POLY_SEL(k)) {
+                            // the clamp keeps the exponent add in range; 2^-126 rounds to 0 in bf16
+                            exp2_poly_pair(pack2(fmaxf(a0, -126.f), fmaxf(a1, -126.f)), y0, y1);
+                        } else {
+                            y0 = ex2_approx(a0);
+                            y1 = ex2_approx(a1);
                         }
-                        tmem_wait_st();
+                        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
+                        pk[k] = pack_bf16x2(y0, y1);
                     }
                 }
-                // P_j as bf16, K-major with 128-byte swizzle: keys [64c, 64c+64) in chunk c
+                float rowsum;
+                {
+                    const uint64_t s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+                    float a0, a1;
+                    unpack2(add2(s01, s23), a0, a1);
+                    rowsum = a0 + a1;
+                }
+                // O_{j-1} is complete here: S_j was issued after PV_{j-1} and has landed
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                    for (int cc = 0; cc < HD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + C::O_COL(t) + cc * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int k = c * 64 + u * 8;
-                        st_shared_v4(sP + c * C::CHUNK + r * 128 + ((u ^ srow_sw) << 4),
-                                     pack_bf16x2(x[k], x[k + 1]), pack_bf16x2(x[k + 2], x[k + 3]),
-                                     pack_bf16x2(x[k + 4], x[k + 5]),
-                                     pack_bf16x2(x[k + 6], x[k + 7]));
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                        tmem_st32(trow + C::O_COL(t) + cc * 32, o);
                     }
-                fence_proxy_async_smem();
+                }
+                {
+                    uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+                    uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+                    tmem_st32(trow + C::S_COL(t), p0);
+                    tmem_st32(trow + C::S_COL(t) + 32, p1);
+                }
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar_pfull);
+                mbar_arrive(bar_p);
                 l = l * alpha + rowsum;
                 m = m_new;
             }
-            if (ok && __all_sync(0xffffffffu, mbar_wait(bar_pvdone, (uint32_t)(n_tiles - 1) & 1u,
-                                                        abort_flag, status))) {
+            if (ok && __all_sync(0xffffffffu, mbar_wait(bar_odone + 8u * t, 0, abort_flag, status))) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                // O / l as bf16 into the (now idle) Q buffer, same swizzled layout as the TMA box
+                // O / l as bf16 into this tile's Q buffer (idle now), in the TMA box layout
 #pragma unroll
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(trow + C::O_COL + cc * 32, o);
+                    tmem_ld32(trow + C::O_COL(t) + cc * 32, o);
                     tmem_wait_ld();
                     const int c = cc >> 1;
 #pragma unroll
@@ -335,7 +528,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
-                        st_shared_v4(sQ + c * C::CHUNK + r * 128 + ((u ^ srow_sw) << 4),
+                        st_shared_v4(sQt + c * C::CHUNK + r * 128 + ((u ^ sw) << 4),
                                      pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
                     }
@@ -343,10 +536,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             }
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (threadIdx.x == 64 && !*abort_flag) {
+        named_barrier_sync(1 + t, 128);
+        if ((threadIdx.x & 127) == 0 && !*abort_flag && qrow0 < T_q) {
 #pragma unroll
-            for (int c = 0; c < C::CH; ++c) tma_store_3d(&tmO, sQ + c * C::CHUNK, head * HD + c * 64, q0, b);
+            for (int c = 0; c < C::CH; ++c)
+                tma_store_3d(&tmO, sQt + c * C::CHUNK, head * HD + c * 64, qrow0, b);
             bulk_commit_group();
             bulk_wait_group<0>();
         }
@@ -392,8 +586,9 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    const dim3 grid((unsigned)(B * h), (unsigned)((T_q + C::BM - 1) / C::BM));
-    attn_bf16_tc_kernel<HD><<<grid, A_THREADS, C::SMEM, stream>>>(tQ, tK, tV, tO, h, T_kv, causal,
+    const int rows_per_cta = C::NQ * C::BM;
+    const dim3 grid((unsigned)(B * h), (unsigned)((T_q + rows_per_cta - 1) / rows_per_cta));
+    attn_bf16_tc_kernel<HD><<<grid, A_THREADS, C::SMEM, stream>>>(tQ, tK, tV, tO, h, T_q, T_kv, causal,
                                                                    kv_lengths, scale_log2, status);
     return cudaGetLastError();
 }

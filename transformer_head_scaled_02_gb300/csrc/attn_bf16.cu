@@ -15,20 +15,26 @@
 // into one FMA per score.
 //
 // Tensor memory (512 columns, one CTA per SM):
-//   S_t  [128 t, 128 t + 128)      scores of query tile t, fp32; once read, the same columns
-//                                  receive P_t as packed bf16 pairs (64 columns)
-//   O_t  [256 + d t, 256 + d t + d) output accumulator of tile t, fp32
-//   Q_t  [384 + 32 t, ...)          (d = 64 only) the query tile itself, packed bf16
-// Both GEMMs read their A operand from TMEM when it lives there (P always; Q for d = 64), so
-// shared memory only feeds the K and V operands.
+//   S_t  [128 t, 128 t + 128)        scores of query tile t, fp32
+//   O_t  [256 + d t, 256 + d t + d)  output accumulator of tile t, fp32
+//   P_t  d = 64:  [384 + 64 t, +64)  probabilities as packed bf16 pairs, own columns
+//        d = 128: the first 64 columns of S_t (TMEM is full: S0, S1, O0, O1 use all 512)
+// The PV product reads P from TMEM (A operand in tensor memory); Q and K come from shared
+// memory.  With its own P columns (d = 64) the scores of key tile j+1 are computed while
+// the softmax of tile j is still running; with P inside S (d = 128) S_{j+1} must wait
+// until P_j has been consumed, and the two query tiles take turns on the tensor core.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a ring of stages;
-//   warp 1      TMEM owner and single-thread MMA issuer.  Per key tile j:
-//                 O_0 += P_0 V_j ; S_0 = Q_0 K_{j+1}^T ; O_1 += P_1 V_j ; S_1 = Q_1 K_{j+1}^T
+//   warp 1      TMEM owner and MMA issuer.  Per key tile j:
+//                 d = 64:  warps 1 and 2 each issue for one query tile t: S_t(j+1) as soon
+//                          as the softmax has read S_t(j), then O_t += P_t V_j as soon as
+//                          P_t is in TMEM;
+//                 d = 128: warp 1 alone, alternating the tiles:
+//                          O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j, S_1(j+1)
 //               (tcgen05 MMAs of one thread execute in issue order, so S_t may overwrite the
 //               P_t columns right after the MMA that reads them);
-//   warps 2-3   idle;
+//   warps 2-3   otherwise idle;
 //   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1 -- one row per thread (TMEM
 //               lane = row): read S, mask, row max, exponentials, row sum, P -> TMEM, lazy
 //               O rescale; while one group works, the tensor core runs the other tile's MMAs.
@@ -62,10 +68,16 @@ struct AttnCfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + BAR_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr bool Q_IN_TMEM = HD == 64;
+    static constexpr bool SEP_P = HD == 64;  // P in its own TMEM columns
+    // MMA-issuing threads: one per query tile when P has its own columns (the tiles' chains
+    // are independent); one for both tiles when P lives in S, where strict alternation
+    // between the tiles keeps the two softmax groups out of phase.
+    static constexpr int ISSUERS = SEP_P ? 2 : 1;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return (uint32_t)(128 * t); }
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return (uint32_t)(256 + HD * t); }
-    __host__ __device__ static constexpr uint32_t Q_COL(int t) { return (uint32_t)(384 + 32 * t); }
+    __host__ __device__ static constexpr uint32_t P_COL(int t) {
+        return SEP_P ? (uint32_t)(384 + 64 * t) : (uint32_t)(128 * t);
+    }
 };
 
 static_assert(AttnCfg<64>::SMEM <= 232448, "smem budget d=64");
@@ -74,9 +86,11 @@ static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 constexpr int A_THREADS = 384;
 
 // Which exponential pairs (of the 64 per row and key tile) go to the FMA-pipe polynomial;
-// the rest use MUFU.  d = 64 has half the MMA work per exponential of d = 128, so it moves
-// more of them off the MUFU unit.
-#define POLY_SEL(k) (HD == 64 ? ((k) % 8 >= 5) : ((k) % 4 == 3))
+// the rest use MUFU.  Measured on GB300, ex2.approx.f32 retires 32 results per clock per SM,
+// which covers a key tile's 32768 exponentials in 1024 clocks -- within the tensor core's
+// time for the same tile at d = 64 and d = 128 -- while the polynomial costs ~4.5 issue slots
+// per value.  So every exponential goes to MUFU.
+#define POLY_SEL(k) false
 
 // Minimax coefficients of 2^f on [-1/2, 1/2] (relative error), degree 3, lowest first.
 constexpr float kExp2C0 = 0.99992806f;
@@ -171,17 +185,17 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const uint32_t sK = sQ + C::NQ * C::Q_BYTES;
     const uint32_t sV = sK + S * C::KV_BYTES;
     const uint32_t sBar = sV + S * C::KV_BYTES;
-    // barriers: q_full, q_tmem, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
-    //           o_done[2], mma_drain
+    // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2],
+    //           pv_done[2], mma_drain
     const uint32_t bar_q = sBar;
-    const uint32_t bar_qtmem = sBar + 8u;
-    const uint32_t bar_kfull = sBar + 16u;
+    const uint32_t bar_kfull = sBar + 8u;
     const uint32_t bar_vfull = bar_kfull + 8u * S;
     const uint32_t bar_kvempty = bar_vfull + 8u * S;
     const uint32_t bar_sfull = bar_kvempty + 8u * S;
-    const uint32_t bar_pfull = bar_sfull + 16u;
-    const uint32_t bar_odone = bar_pfull + 16u;
-    const uint32_t bar_drain = bar_odone + 16u;
+    const uint32_t bar_sfree = bar_sfull + 16u;
+    const uint32_t bar_pfull = bar_sfree + 16u;
+    const uint32_t bar_pvdone = bar_pfull + 16u;
+    const uint32_t bar_drain = bar_pvdone + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -210,18 +224,18 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
-        mbar_init(bar_qtmem, 256);
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_kfull + 8u * s, 1);
             mbar_init(bar_vfull + 8u * s, 1);
-            mbar_init(bar_kvempty + 8u * s, 1);
+            mbar_init(bar_kvempty + 8u * s, C::ISSUERS);  // one commit per MMA-issuing thread
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_sfull + 8u * t, 1);
+            mbar_init(bar_sfree + 8u * t, 128);
             mbar_init(bar_pfull + 8u * t, 128);
-            mbar_init(bar_odone + 8u * t, 1);
+            mbar_init(bar_pvdone + 8u * t, 1);
         }
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, C::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
         if (bad) record_status(status, kStatusBadLength);
@@ -274,91 +288,152 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 drain_wait_a(bar_vfull + 8u * st, ph);
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0 && n_max > 0) {
-            // ---------------- MMA issuer
+    } else if (C::ISSUERS == 2 && (warp == 1 || warp == 2)) {
+        if (lane == 0) {
+            // ---------------- MMA issuers: warp 1 for query tile 0, warp 2 for tile 1.
+            // tcgen05.mma issue is paced by the tensor core (the issuing thread stalls while
+            // its queue is full), so every wait/commit between MMA batches of one thread is
+            // a bubble; with one issuing thread per tile, one thread's waits overlap the
+            // other's MMAs.  The tiles are independent (own TMEM columns); both threads read
+            // the same K/V stages and each commits once per key tile to release a stage.
+            const int t = warp - 1;
+            const int n = n_t[t];
             // Descriptors are built once; per MMA only the start-address field changes, by
             // adding the (16-byte granular) offset of the K step to the stage's descriptor.
             const uint32_t idesc_s = idesc_bf16_f32(128, C::BN, false, false);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
             const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sV, C::CHUNK, 1024);
-            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
-            bool ok = mbar_wait(bar_q, 0, abort_flag, status);
-            if (C::Q_IN_TMEM) ok = ok && mbar_wait(bar_qtmem, 0, abort_flag, status);
-            int k_ready = -1;  // highest key tile whose K has been waited for
-            if (ok) {
-                ok = mbar_wait(bar_kfull, 0, abort_flag, status);
-                k_ready = 0;
-            }
-            if (ok) {
-                tc_fence_after();
+            const uint64_t qdesc = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+            // S_t = Q_t K_j^T into S_t's columns, then signal s_full_t
+            auto issue_s = [&](int j) {
+                const uint64_t kdesc = kdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (n_t[t] == 0) continue;
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
+                    mma_bf16_ss(tmem_base + C::S_COL(t), qdesc + off16, kdesc + off16, idesc_s,
+                                kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar_sfull + 8u * t);
+            };
+            // O_t += P_t V_j, then signal pv_done_t
+            auto issue_pv = [&](int j) {
+                const uint64_t vdesc = vdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
-                        if (C::Q_IN_TMEM)
-                            mma_bf16_ts(tmem_base + C::S_COL(t), tmem_base + C::Q_COL(t) + kk * 8,
-                                        kdesc0 + off16, idesc_s, kk > 0 ? 1u : 0u);
-                        else
-                            mma_bf16_ss(tmem_base + C::S_COL(t),
-                                        qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4) + off16,
-                                        kdesc0 + off16, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar_sfull + 8u * t);
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::P_COL(t) + kk * 8,
+                                vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar_pvdone + 8u * t);
+            };
+            auto wait_k = [&](int j) {
+                return mbar_wait(bar_kfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
+            };
+            bool ok = true;
+            if (n > 0) {
+                ok = mbar_wait(bar_q, 0, abort_flag, status) && wait_k(0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
                 }
             }
-            for (int j = 0; j < n_max && ok; ++j) {
-                const int st = j % S;
-                if (!mbar_wait(bar_vfull + 8u * st, (uint32_t)(j / S) & 1u, abort_flag, status)) break;
-                const uint64_t vdesc = vdesc0 + (uint64_t)((st * C::KV_BYTES) >> 4);
+            int j = 0;
+            for (; j < n && ok; ++j) {
                 const int jn = j + 1;
-                const uint64_t kdesc = kdesc0 + (uint64_t)(((jn % S) * C::KV_BYTES) >> 4);
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= n_t[t]) continue;
-                    if (!mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status)) {
+                if (C::SEP_P && jn < n) {
+                    // next scores first: only the softmax's read of S_t(j) gates them
+                    ok = wait_k(jn) &&
+                         mbar_wait(bar_sfree + 8u * t, (uint32_t)j & 1u, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(jn);
+                }
+                ok = mbar_wait(bar_vfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status) &&
+                     mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(j);
+                if (!C::SEP_P && jn < n) {
+                    // P_t lives in S_t's columns: S_t(j+1) goes after the PV that reads P_t(j)
+                    if (!wait_k(jn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    issue_s(jn);
+                }
+                tc_commit(bar_kvempty + 8u * (j % S));
+            }
+            // release the stages of key tiles this query tile does not use (the other tile
+            // may need one more key tile under the causal mask)
+            if (ok)
+                for (; j < n_max; ++j) tc_commit(bar_kvempty + 8u * (j % S));
+            tc_commit(bar_drain);
+            drain_wait_a(bar_drain, 0);
+        }
+    } else if (C::ISSUERS == 1 && warp == 1) {
+        if (lane == 0) {
+            // ---------------- single MMA issuer for both query tiles, strictly alternating:
+            //   O_0 += P_0 V_j ; S_0(j+1) ; O_1 += P_1 V_j ; S_1(j+1)
+            const uint32_t idesc_s = idesc_bf16_f32(128, C::BN, false, false);
+            const uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
+            const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sV, C::CHUNK, 1024);
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+            auto issue_s = [&](int t, int j) {
+                const uint64_t kdesc = kdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
+                const uint64_t qdesc = qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; ++kk)
-                        mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::S_COL(t) + kk * 8,
-                                    vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
+                    mma_bf16_ss(tmem_base + C::S_COL(t), qdesc + off16, kdesc + off16, idesc_s,
+                                kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar_sfull + 8u * t);
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint64_t vdesc = vdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::P_COL(t) + kk * 8,
+                                vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar_pvdone + 8u * t);
+            };
+            bool ok = true;
+            if (n_max > 0) {
+                ok = mbar_wait(bar_q, 0, abort_flag, status) &&
+                     mbar_wait(bar_kfull, 0, abort_flag, status);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t)
+                        if (n_t[t] > 0) issue_s(t, 0);
+                }
+            }
+            int k_ready = 0;  // highest key tile whose K has been waited for
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int jn = j + 1;
+                ok = mbar_wait(bar_vfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
+#pragma unroll
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= n_t[t]) continue;
+                    ok = mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, j);
                     if (jn < n_t[t]) {
                         if (jn > k_ready) {
-                            if (!mbar_wait(bar_kfull + 8u * (jn % S), (uint32_t)(jn / S) & 1u,
-                                           abort_flag, status)) {
-                                ok = false;
-                                break;
-                            }
+                            ok = mbar_wait(bar_kfull + 8u * (jn % S), (uint32_t)(jn / S) & 1u,
+                                           abort_flag, status);
                             k_ready = jn;
+                            if (!ok) break;
                             tc_fence_after();
                         }
-#pragma unroll
-                        for (int kk = 0; kk < HD / 16; ++kk) {
-                            const uint32_t off16 =
-                                (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
-                            if (C::Q_IN_TMEM)
-                                mma_bf16_ts(tmem_base + C::S_COL(t),
-                                            tmem_base + C::Q_COL(t) + kk * 8, kdesc + off16, idesc_s,
-                                            kk > 0 ? 1u : 0u);
-                            else
-                                mma_bf16_ss(tmem_base + C::S_COL(t),
-                                            qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4) + off16,
-                                            kdesc + off16, idesc_s, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(bar_sfull + 8u * t);
-                    } else {
-                        tc_commit(bar_odone + 8u * t);
+                        issue_s(t, jn);
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar_kvempty + 8u * st);
+                tc_commit(bar_kvempty + 8u * (j % S));
             }
             tc_commit(bar_drain);
             drain_wait_a(bar_drain, 0);
@@ -376,27 +451,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         const uint32_t sQt = sQ + t * C::Q_BYTES;
         const uint32_t bar_s = bar_sfull + 8u * t, bar_p = bar_pfull + 8u * t;
         bool ok = true;
-
-        if (C::Q_IN_TMEM && n_max > 0) {
-            // Q row -> TMEM (packed bf16 pairs, 32 columns) for the TMEM-operand score MMA
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag, status));
-            if (ok) {
-                uint32_t qv[32];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        gbase + (sQt - base) + r * 128 + ((u ^ sw) << 4));
-                    qv[4 * u] = v.x;
-                    qv[4 * u + 1] = v.y;
-                    qv[4 * u + 2] = v.z;
-                    qv[4 * u + 3] = v.w;
-                }
-                tmem_st32(trow + C::Q_COL(t), qv);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(bar_qtmem);
-        }
 
         if (n == 0) {
             // no valid key: the softmax is undefined, the rows are NaN
@@ -423,6 +477,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(trow + C::S_COL(t) + c * 32, sr[c]);
                     tmem_wait_ld();
+                    if (C::SEP_P) {
+                        // S_t(j) is in registers: the MMA warp may compute S_t(j+1) now
+                        tc_fence_before();
+                        mbar_arrive(bar_sfree + 8u * t);
+                    }
 #pragma unroll
                     for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
                 }
@@ -487,7 +546,16 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     unpack2(add2(s01, s23), a0, a1);
                     rowsum = a0 + a1;
                 }
-                // O_{j-1} is complete here: S_j was issued after PV_{j-1} and has landed
+                if (C::SEP_P && j > 0) {
+                    // PV_t(j-1) done: O_t is stable and the P_t columns are free
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone + 8u * t, (uint32_t)(j - 1) & 1u,
+                                                           abort_flag, status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                // (P inside S: S_t(j) was issued after PV_t(j-1), so O_t is already complete)
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float a = rescale ? alpha : 1.f;
 #pragma unroll
@@ -503,8 +571,8 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 {
                     uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
                     uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-                    tmem_st32(trow + C::S_COL(t), p0);
-                    tmem_st32(trow + C::S_COL(t) + 32, p1);
+                    tmem_st32(trow + C::P_COL(t), p0);
+                    tmem_st32(trow + C::P_COL(t) + 32, p1);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -512,7 +580,8 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 l = l * alpha + rowsum;
                 m = m_new;
             }
-            if (ok && __all_sync(0xffffffffu, mbar_wait(bar_odone + 8u * t, 0, abort_flag, status))) {
+            if (ok && __all_sync(0xffffffffu, mbar_wait(bar_pvdone + 8u * t, (uint32_t)(n - 1) & 1u,
+                                                        abort_flag, status))) {
                 tc_fence_after();
                 const float inv = 1.f / l;
                 // O / l as bf16 into this tile's Q buffer (idle now), in the TMA box layout

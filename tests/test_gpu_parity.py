@@ -125,6 +125,29 @@ def test_attention_step_bf16(B, T_q, T_kv, h, d, causal, lengths, scale):
     assert_close(to_host(O), ref, "bf16", f"attention {B}x{T_q}x{T_kv} h{h} d{d}")
 
 
+@pytest.mark.parametrize("ramp_top", [12.0, 40.0])
+@pytest.mark.parametrize("d,causal", [(64, True), (64, False), (128, True), (128, False)])
+def test_attention_growing_scores_bf16(d, causal, ramp_top):
+    """Scores that grow steeply along the keys: each key tile's maximum is far above the
+    previous tiles'.  With the steeper ramp later tiles exceed the first tile's maximum by
+    far more than 64 (in base-2 units), so the kernel must leave its no-maximum fast path,
+    move its reference maximum and rescale O and the row sums."""
+    B, T, h = 1, 640, 2
+    Q = wl.random_tensor((B, T, h * d), seed=30, scale=1.0)
+    Kb = wl.random_tensor((B, T, h * d), seed=31, scale=1.0)
+    ramp = (0.2 + ramp_top * np.arange(T, dtype=np.float32) / T)[None, :, None]
+    K = wl.round_to_bf16(Kb * ramp)
+    V = wl.random_tensor((B, T, h * d), seed=32)
+    layer = Mha(h * d, h, d, dtype=torch.bfloat16)
+    layer.ensure_workspace(1, 1, 1)
+    O = layer.attention(to_device(Q, "bf16"), to_device(K, "bf16"), to_device(V, "bf16"),
+                        causal=causal)
+    torch.cuda.synchronize()
+    assert layer.status() == _lib.MHA_OK
+    ref = oracle.attention(Q, K, V, h=h, causal=causal)
+    assert_close(to_host(O), ref, "bf16", f"growing scores d{d} causal={causal}")
+
+
 @pytest.mark.parametrize("B,T_q,T_kv,h,dk,dv,causal,lengths", [
     (1, 16, 16, 8, 4, 4, False, None),
     (2, 77, 77, 3, 16, 8, True, None),

@@ -40,15 +40,14 @@
 //               O rescale; while one group works, the tensor core runs the other tile's MMAs.
 //               At the end O/l is rounded to bf16 and stored by TMA straight into column
 //               block (head * d) of the (B, T, h*d) Concat output.
-// The rescale is lazy: the reference maximum moves only when a tile's maximum exceeds it by
-// more than 8 (a factor 256 in base 2); numerator and denominator share the reference, so the
-// final O/l is unchanged.
-// exp2: three quarters of the exponentials go to the MUFU unit (ex2.approx); one quarter is
-// computed on the FMA pipe -- x = n + f with n = round(x) by the 1.5*2^23 magic-number add,
-// 2^f by a degree-3 polynomial whose coefficients are the minimax (relative error, Remez
-// exchange) fit of 2^f on [-1/2, 1/2], max relative error 7.5e-5, and 2^n added into the
-// exponent field.  P is rounded to bf16 (relative step 2^-9) right after, so the polynomial
-// error is invisible.  Tiles with masked entries use MUFU only, so masked weights are exactly 0.
+// Reference maximum: P = 2^(s*c - m_ref) gives the same O / l for any reference m_ref (the
+// numerator and the denominator carry the same factor); the reference only has to keep P
+// finite.  So the first key tile sets m_ref to the exact row maximum, and later tiles skip
+// the maximum altogether: their P is computed against the current m_ref and only if a row's
+// sum exceeds 2^64 (or is not finite) does the warp redo the tile with the exact maximum and
+// rescale O and l.  Every exponential runs on the MUFU unit (ex2.approx), which retires 32
+// results per clock per SM on GB300 -- a key tile's 32768 exponentials in 1024 clocks, within
+// the tensor core's time for the same tile.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -85,18 +84,7 @@ static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 
 constexpr int A_THREADS = 384;
 
-// Which exponential pairs (of the 64 per row and key tile) go to the FMA-pipe polynomial;
-// the rest use MUFU.  Measured on GB300, ex2.approx.f32 retires 32 results per clock per SM,
-// which covers a key tile's 32768 exponentials in 1024 clocks -- within the tensor core's
-// time for the same tile at d = 64 and d = 128 -- while the polynomial costs ~4.5 issue slots
-// per value.  So every exponential goes to MUFU.
-#define POLY_SEL(k) false
 
-// Minimax coefficients of 2^f on [-1/2, 1/2] (relative error), degree 3, lowest first.
-constexpr float kExp2C0 = 0.99992806f;
-constexpr float kExp2C1 = 0.69326097f;
-constexpr float kExp2C2 = 0.24261113f;
-constexpr float kExp2C3 = 0.05517167f;
 
 __device__ __forceinline__ void drain_wait_a(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -145,26 +133,55 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
+
+
+// One row of a 128-key score tile from TMEM into registers (warp-collective), with the
+// causal / key-length mask applied (keys [0, lim) are visible).
+__device__ __forceinline__ void load_s_tile(uint32_t taddr, bool masked, int kv0, int lim,
+                                            float (&x)[128]) {
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, sr[c]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+    if (masked) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+            if (kv0 + c >= lim) x[c] = -INFINITY;
+    }
 }
 
-// 2^x for a pair of finite x >= -126 on the FMA pipe (see the top of the file).
-__device__ __forceinline__ void exp2_poly_pair(uint64_t x, float& y0, float& y1) {
-    const uint64_t magic = pack2(12582912.0f, 12582912.0f);
-    const uint64_t t = add2(x, magic);   // round-to-nearest integer in the low mantissa bits
-    const uint64_t n = sub2(t, magic);
-    const uint64_t f = sub2(x, n);       // f in [-1/2, 1/2]
-    uint64_t p = fma2(pack2(kExp2C3, kExp2C3), f, pack2(kExp2C2, kExp2C2));
-    p = fma2(p, f, pack2(kExp2C1, kExp2C1));
-    p = fma2(p, f, pack2(kExp2C0, kExp2C0));
-    float p0, p1, t0, t1;
-    unpack2(p, p0, p1);
-    unpack2(t, t0, t1);
-    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+// Row maximum of a score tile: 8 independent chains of 3-input max.
+__device__ __forceinline__ float row_max(const float (&x)[128]) {
+    float mk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mk[k] = x[k];
+#pragma unroll
+    for (int c = 8; c < 128; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + k], x[c + 8 + k]);
+    return fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+}
+
+// p = 2^(s*c + neg) for the 128 scores of a row; returns the row sum (fp32, 4 packed partial
+// sums) and writes P as packed bf16 pairs.
+__device__ __forceinline__ float exp_tile(const float (&x)[128], uint64_t c2, float neg,
+                                          uint32_t (&pk)[64]) {
+    const uint64_t neg2 = pack2(neg, neg);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+        float a0, a1;
+        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
+        const float y0 = ex2_approx(a0), y1 = ex2_approx(a1);
+        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
+        pk[k] = pack_bf16x2(y0, y1);
+    }
+    const uint64_t s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+    float a0, a1;
+    unpack2(add2(s01, s23), a0, a1);
+    return a0 + a1;
 }
 
 template <int HD>
@@ -463,7 +480,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         } else {
             float m = -INFINITY;  // reference maximum, already scaled to base 2
             float l = 0.f;
-            const uint64_t c2 = pack2(scale_log2, scale_log2);
+            float x[128];
             for (int j = 0; j < n && ok; ++j) {
                 // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)j & 1u, abort_flag, status))) {
@@ -471,80 +488,33 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                float x[128];
-                {
-                    uint32_t sr[4][32];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(trow + C::S_COL(t) + c * 32, sr[c]);
-                    tmem_wait_ld();
-                    if (C::SEP_P) {
-                        // S_t(j) is in registers: the MMA warp may compute S_t(j+1) now
-                        tc_fence_before();
-                        mbar_arrive(bar_sfree + 8u * t);
-                    }
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-                }
                 const int kv0 = j * C::BN;
                 const bool masked = kv0 + C::BN > L || (causal && kv0 + C::BN - 1 > qrow0);
-                if (masked) {
-                    const int lim = causal ? min(L, row + 1) : L;  // keys [0, lim) are visible
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (kv0 + c >= lim) x[c] = -INFINITY;
-                }
-                // row maximum: 8 independent chains of 3-input max
-                float mk[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mk[k] = x[k];
-#pragma unroll
-                for (int c = 8; c < 128; c += 16)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + k], x[c + 8 + k]);
-                const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
-                                       fmaxf(mk[6], mk[7]));
-                const float m_tile = mx * scale_log2;
-                float m_new = m;
-                if (m_tile > m + 8.0f) m_new = m_tile;
-                const bool rescale = (m_new != m) && j > 0;
-                const float alpha = ex2_approx(m - m_new);
-                const float neg = m_new == -INFINITY ? 0.f : -m_new;
-                const uint64_t neg2 = pack2(neg, neg);
-
-                // exponentials, row sum (4 packed partial sums), P as packed bf16
+                const int lim = causal ? min(L, row + 1) : L;  // keys [0, lim) are visible
                 uint32_t pk[64];
-                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-                if (masked) {
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) {
-                        float a0, a1;
-                        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
-                        const float y0 = ex2_approx(a0), y1 = ex2_approx(a1);
-                        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
-                        pk[k] = pack_bf16x2(y0, y1);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) {
-                        float a0, a1, y0, y1;
-                        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
-                        if (POLY_SEL(k)) {
-                            // the clamp keeps the exponent add in range; 2^-126 rounds to 0 in bf16
-                            exp2_poly_pair(pack2(fmaxf(a0, -126.f), fmaxf(a1, -126.f)), y0, y1);
-                        } else {
-                            y0 = ex2_approx(a0);
-                            y1 = ex2_approx(a1);
-                        }
-                        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
-                        pk[k] = pack_bf16x2(y0, y1);
-                    }
+                float rowsum, alpha = 1.f, m_new = m;
+                // Fast path (every key tile after the first): no row maximum.  P is computed
+                // against the current reference m; any reference gives the same O / l, it only
+                // has to keep P finite.  If some row's sum exceeds 2^64 (or is not finite) the
+                // warp redoes the tile with the exact maximum (slow path, also used for j = 0).
+                bool slow = j == 0;
+                if (!slow) {
+                    load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
+                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), -m, pk);
+                    slow = !__all_sync(0xffffffffu, rowsum <= 18446744073709551616.f);
                 }
-                float rowsum;
-                {
-                    const uint64_t s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
-                    float a0, a1;
-                    unpack2(add2(s01, s23), a0, a1);
-                    rowsum = a0 + a1;
+                if (slow) {
+                    load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
+                    const float m_tile = row_max(x) * scale_log2;
+                    m_new = m_tile > m ? m_tile : m;
+                    alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), m_new == -INFINITY ? 0.f : -m_new, pk);
+                }
+                const bool rescale = (m_new != m) && j > 0;
+                if (C::SEP_P) {
+                    // S_t(j) is no longer needed: the MMA warp may compute S_t(j+1) now
+                    tc_fence_before();
+                    mbar_arrive(bar_sfree + 8u * t);
                 }
                 if (C::SEP_P && j > 0) {
                     // PV_t(j-1) done: O_t is stable and the P_t columns are free

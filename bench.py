@@ -182,38 +182,42 @@ def to_device(a, dtype_name, torch):
 
 
 def cpu_baseline(w, budget_s: float = 15.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload: batch 0
-    and its first T' query rows (for causal self-attention the outputs of those rows
-    depend on nothing else), T' sized to take about budget_s on the host cores."""
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: the first nb
+    batches and, of each, the first T' query rows (for causal self-attention the outputs of
+    those rows depend on nothing else).  The sample grows (rows first, then batches, up to
+    the whole workload) until one run takes about a quarter of budget_s or more."""
     import oracle
     oracle.build()
     x = wl.make_inputs(w)
 
-    def run(tp):
-        sub = dict(X_q=x["X_q"][:1, :tp], W_qkv=x["W_qkv"], b_qkv=x["b_qkv"], W_o=x["W_o"],
-                   b_o=x["b_o"])
+    def run(nb, tp):
         t0 = time.perf_counter()
         if w.cross:
-            L = None if x["kv_lengths"] is None else x["kv_lengths"][:1]
-            oracle.mha_forward(sub["X_q"], sub["W_qkv"], sub["b_qkv"], sub["W_o"], sub["b_o"], w.h,
-                               w.d_k, w.d_v, Xkv=x["X_kv"][:1], causal=w.causal, kv_lengths=L)
+            L = None if x["kv_lengths"] is None else x["kv_lengths"][:nb]
+            oracle.mha_forward(x["X_q"][:nb, :tp], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h,
+                               w.d_k, w.d_v, Xkv=x["X_kv"][:nb], causal=w.causal, kv_lengths=L)
         else:
-            oracle.mha_forward(sub["X_q"], sub["W_qkv"], sub["b_qkv"], sub["W_o"], sub["b_o"], w.h,
+            oracle.mha_forward(x["X_q"][:nb, :tp], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h,
                                w.d_k, w.d_v, causal=w.causal)
         return time.perf_counter() - t0
 
-    tp = min(w.T_q, 64)
-    dt = run(tp)
-    while tp < w.T_q and dt < budget_s / 4:
-        tp = min(w.T_q, tp * 2)
-        dt = run(tp)
-    sw = wl.custom("sample", B=1, T_q=tp, T_kv=w.T_kv if w.cross else tp, D=w.D, h=w.h, d_k=w.d_k,
-                   d_v=w.d_v, dtype=w.dtype, causal=w.causal, cross=w.cross)
+    nb, tp = 1, min(w.T_q, 64)
+    dt = run(nb, tp)
+    while dt < budget_s / 4 and (tp < w.T_q or nb < w.B):
+        if tp < w.T_q:
+            tp = min(w.T_q, tp * 2)
+        else:
+            nb = min(w.B, nb * 2)
+        dt = run(nb, tp)
+    sw = wl.custom("sample", B=nb, T_q=tp, T_kv=w.T_kv if w.cross else tp, D=w.D, h=w.h,
+                   d_k=w.d_k, d_v=w.d_v, dtype=w.dtype, causal=w.causal, cross=w.cross)
     f = wl.flops(sw)["total"]
+    whole = nb == w.B and tp == w.T_q
+    what = ("the whole workload" if whole else
+            f"batches 0..{nb - 1}, first {tp} of {w.T_q} query rows of {w.name}")
     return {"value": f / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"batch 0, first {tp} of {w.T_q} query rows of {w.name} "
-                      f"({'all ' + str(w.T_kv) + ' keys' if w.cross else 'causal prefix'}), fp64, "
-                      f"{dt:.2f} s"}
+            "sample": f"{what} ({'all ' + str(w.T_kv) + ' keys' if w.cross else 'causal prefix'}), "
+                      f"fp64, {dt:.2f} s"}
 
 
 def run_ours(args):

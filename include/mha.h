@@ -159,6 +159,19 @@ mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv,
  */
 mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream);
 
+/*
+ * mha_check_wait_timeout -- exercise the failure path of the kernels' pipeline waits.  (The
+ * pages have no counterpart: this is the library's own failure detection.)  Every wait on a
+ * pipeline barrier inside the kernels gives up after one second, records MHA_ERR_TIMEOUT in
+ * the workspace status word and lets the kernel drain and exit instead of hanging.  This call
+ * launches one small kernel whose waits are on a barrier that nothing ever completes, with
+ * the given limit (1 ns .. 10 s), so a test can check that the timeout is reported through
+ * mha_get_status and that the CUDA context stays usable.  Needs an attached workspace
+ * (MHA_ERR_WORKSPACE otherwise); MHA_ERR_INVALID_ARG for a NULL handle or a limit out of
+ * range.  Asynchronous on `stream`.
+ */
+mha_status mha_check_wait_timeout(mha_t handle, int64_t limit_ns, void* stream);
+
 /* mha_strerror -- static description of a status code. */
 const char* mha_strerror(mha_status status);
 

@@ -103,3 +103,14 @@ def test_linear_and_attention_reject_bad_arguments(lib):
         assert att(T_q=0) == L.MHA_OK
     finally:
         L.mha_destroy(bf)
+
+
+def test_wait_probe_rejects_bad_arguments(lib):
+    hdl = L.mha_create(256, 4, 64, 64, L.MHA_BF16)
+    try:
+        assert L.mha_check_wait_timeout(None, 1000, None, check=False) == L.MHA_ERR_INVALID_ARG
+        assert L.mha_check_wait_timeout(hdl, 0, None, check=False) == L.MHA_ERR_INVALID_ARG
+        assert L.mha_check_wait_timeout(hdl, 20_000_000_000, None, check=False) == L.MHA_ERR_INVALID_ARG
+        assert L.mha_check_wait_timeout(hdl, 1000, None, check=False) == L.MHA_ERR_WORKSPACE
+    finally:
+        L.mha_destroy(hdl)

@@ -42,6 +42,7 @@ _SIGNATURES = {
     "mha_get_status": (_i, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "mha_forward_static_workspace": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp,
                                           _vp, _vp]),
+    "mha_check_wait_timeout": (_i, [_vp, _i64, _vp]),
     "mha_strerror": (ctypes.c_char_p, [_i]),
 }
 
@@ -129,6 +130,12 @@ def mha_get_status(handle: int, stream: int) -> int:
     v = ctypes.c_int32(0)
     _check("mha_get_status", load().mha_get_status(handle, ctypes.byref(v), stream))
     return int(v.value)
+
+
+def mha_check_wait_timeout(handle: int, limit_ns: int, stream, check: bool = True) -> int:
+    """Run the kernels' bounded barrier wait against a barrier that never completes."""
+    code = load().mha_check_wait_timeout(handle, limit_ns, stream)
+    return _check("mha_check_wait_timeout", code) if check else code
 
 
 MHA_STATIC_WORKSPACE_BYTES = 32 << 20

@@ -256,6 +256,252 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// CTA-pair version (cta_group::2): a cluster of two CTAs on two SMs computes a 256x256
+// output tile with M = 256 MMAs.  Each CTA stages its own 128 rows of A and 128 of the 256
+// columns of B, so per SM the operand traffic through shared memory is A 4 KB + B 4 KB per
+// 128-clock MMA instead of A 4 KB + B 8 KB (plus the TMA fills, likewise halved for B): the
+// one-SM kernel above is bound by shared-memory bandwidth at about two thirds of the tensor
+// rate; the pair is not.
+//   warp 0 (both CTAs)   TMA: own A rows and own half of B, completing on the even CTA's
+//                        stage barrier (which expects both CTAs' bytes);
+//   warp 1               TMEM owner (pair allocation) and, in the even CTA only, the single
+//                        MMA issuer; its commits are multicast to both CTAs' barriers;
+//   warps 2..5 (both)    epilogue of the CTA's own 128 rows, as above; they release the
+//                        accumulator by arriving on the even CTA's barrier.
+constexpr int P_BK = 64;
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * P_BK * 2;          // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_CHUNK = P_BK * 64 * 2;           // 8 KB: 64 K-rows x 64 N-columns
+constexpr int P_B_BYTES = P_BK * 128 * 2;          // 16 KB: this CTA's half of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + 1024;
+
+static_assert(P_SMEM <= 232448, "shared memory budget (pair)");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
+    gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmW,
+                          const __grid_constant__ CUtensorMap tmC,
+                          const __nv_bfloat16* __restrict__ bias, int M, int N, int K,
+                          int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + P_STAGES * P_A_BYTES;
+    const uint32_t sE = sB + P_STAGES * P_B_BYTES;
+    const uint32_t sBar = sE + G_EPI_BYTES;
+    // barrier layout (same offsets in both CTAs): full[S], empty[S], tfull[2], tempty[2], drain
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8u * P_STAGES;
+    const uint32_t bar_tfull = sBar + 16u * P_STAGES;
+    const uint32_t bar_tempty = bar_tfull + 16u;
+    const uint32_t bar_drain = bar_tempty + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = (int)(blockIdx.x >> 1);
+    const int npairs = (int)(gridDim.x >> 1);
+    const int num_m = (M + 255) / 256;
+    const int num_n = (N + G_BN - 1) / G_BN;
+    const int num_tiles = num_m * num_n;
+    const int num_k = (K + P_BK - 1) / P_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(bar_full + 8u * s, 1);   // used in the even CTA: its producer's arrival
+            mbar_init(bar_empty + 8u * s, 1);  // one multicast commit per use of the stage
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8u * a, 1);
+            mbar_init(bar_tempty + 8u * a, 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), G_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                const int m0 = (tile % num_m) * 256 + (int)rank * 128;
+                const int nb = (tile / num_m) * G_BN + (int)rank * 128;
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(bar_full + 8u * stage, 0);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8u * stage, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(sA + stage * P_A_BYTES, &tmA, kb * P_BK, m0, fb);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_2d_pair(sB + stage * P_B_BYTES + c * P_B_CHUNK, &tmW, nb + c * 64,
+                                         kb * P_BK, fb);
+                    ++issued;
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // the even CTA waits for every stage it expected (its own and the odd CTA's
+            // copies); the odd CTA's copies land before that barrier completes
+            if (leader)
+                for (int back = 0; back < P_STAGES && back < issued; ++back) {
+                    stage = stage == 0 ? P_STAGES - 1 : stage - 1;
+                    if (stage == P_STAGES - 1) phase ^= 1u;
+                    drain_wait(bar_full + 8u * stage, phase);
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (even CTA only)
+            const uint32_t idesc = idesc_bf16_f32(256, G_BN, false, true);
+            const uint64_t adesc0 = sdesc_sw128(sA, 16, 1024);
+            const uint64_t bdesc0 = sdesc_sw128(sB, P_B_CHUNK, 1024);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(bar_tempty + 8u * acc, acc_phase ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * G_BN);
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_full + 8u * stage, phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = adesc0 + (uint64_t)((stage * P_A_BYTES) >> 4);
+                    const uint64_t bd = bdesc0 + (uint64_t)((stage * P_B_BYTES) >> 4);
+#pragma unroll
+                    for (int k = 0; k < P_BK / 16; ++k)
+                        mma_bf16_ss_pair(d_tmem, ad + (uint64_t)((k * 32) >> 4),
+                                         bd + (uint64_t)((k * 2048) >> 4), idesc,
+                                         (kb | k) != 0 ? 1u : 0u);
+                    tc_commit_pair_mc(bar_empty + 8u * stage, 0x3);
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(bar_tfull + 8u * acc, 0x3);
+            }
+            // all MMAs complete before either CTA releases its TMEM or shared memory
+            tc_commit_pair_mc(bar_drain, 0x1);
+            drain_wait(bar_drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: this CTA's 128 rows, one TMEM lane per thread
+        const int q = warp & 3;
+        const int e = warp - 2;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint32_t bufsel = 0;
+        int it = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
+            const int m0 = (tile % num_m) * 256 + (int)rank * 128;
+            const int n0 = (tile / num_m) * G_BN;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
+                break;
+            tc_fence_after();
+            const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
+#pragma unroll 1
+            for (int c = 0; c < G_BN / 64; ++c) {
+                uint32_t v[2][32];
+                tmem_ld32(t0 + c * 64, v[0]);
+                tmem_ld32(t0 + c * 64 + 32, v[1]);
+                tmem_wait_ld();
+                if (c == G_BN / 64 - 1) {
+                    // accumulator fully read: release it to the MMA issuer in the even CTA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(bar_tempty + 8u * acc);
+                        else
+                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * acc, 0));
+                    }
+                }
+                const int nc = n0 + c * 64;
+                if (nc >= N || m0 + q * 32 >= M) continue;  // sub-tile wholly outside C
+                const uint32_t buf = sE + (uint32_t)((e * 2 + (int)bufsel) * G_EPI_BUF);
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t row = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
+                    if (bias != nullptr && nc + u * 8 < N) {
+                        const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
+                        const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            x[2 * i] += __uint_as_float(bw[i] << 16);
+                            x[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
+                        }
+                    }
+                    st_shared_v4(row + ((uint32_t)(u ^ (lane & 7)) << 4), pack_bf16x2(x[0], x[1]),
+                                 pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                                 pack_bf16x2(x[6], x[7]));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmC, buf, nc, m0 + q * 32);
+                    bulk_commit_group();
+                }
+                bufsel ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the pair's MMAs may touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, G_TMEM_COLS);
+    }
+}
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
@@ -280,10 +526,44 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         const uint32_t box[2] = {64, 32};
         if (!encode_tmap_bf16(&tC, C, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
+    const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
+    if (M > 128) {
+        // CTA pairs: the W box is 64 columns x 64 K-rows, the A box 64 K x 128 rows (as
+        // above); each CTA of a pair loads its own A rows and its half of the W tile.
+        cudaError_t err = cudaFuncSetAttribute(gemm_bf16_pair_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+        if (err != cudaSuccess) return err;
+        static int max_pairs_cache[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int max_pairs = dev >= 0 && dev < 64 ? max_pairs_cache[dev] : 0;
+        if (max_pairs == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
+            cfg.blockDim = dim3(G_THREADS);
+            cfg.dynamicSmemBytes = P_SMEM;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+                n = num_sms / 2;
+            max_pairs = n;
+            if (dev >= 0 && dev < 64) max_pairs_cache[dev] = n;
+        }
+        const int pair_tiles = ((M + 255) / 256) * ((N + G_BN - 1) / G_BN);
+        const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+        gemm_bf16_pair_kernel<<<2 * pairs, G_THREADS, P_SMEM, stream>>>(
+            tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
+        return cudaGetLastError();
+    }
     cudaError_t err = cudaFuncSetAttribute(gemm_bf16_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (err != cudaSuccess) return err;
-    const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
     const int grid = num_tiles < num_sms ? num_tiles : num_sms;
     gemm_bf16_tc_kernel<<<grid, G_THREADS, G_SMEM, stream>>>(
         tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);

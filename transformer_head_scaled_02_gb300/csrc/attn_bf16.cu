@@ -480,7 +480,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         } else {
             float m = -INFINITY;  // reference maximum, already scaled to base 2
             float l = 0.f;
-            float x[128];
             for (int j = 0; j < n && ok; ++j) {
                 // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)j & 1u, abort_flag, status))) {
@@ -492,30 +491,43 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 const bool masked = kv0 + C::BN > L || (causal && kv0 + C::BN - 1 > qrow0);
                 const int lim = causal ? min(L, row + 1) : L;  // keys [0, lim) are visible
                 uint32_t pk[64];
+                float x[128];
                 float rowsum, alpha = 1.f, m_new = m;
-                // Fast path (every key tile after the first): no row maximum.  P is computed
-                // against the current reference m; any reference gives the same O / l, it only
-                // has to keep P finite.  If some row's sum exceeds 2^64 (or is not finite) the
-                // warp redoes the tile with the exact maximum (slow path, also used for j = 0).
-                bool slow = j == 0;
-                if (!slow) {
+                if constexpr (C::SEP_P) {
+                    // P has its own columns: S_t(j) is released right after it is read, so the
+                    // scores of the next key tile are computed while this softmax runs.  The
+                    // tile maximum is always computed; the reference moves only when it would
+                    // otherwise let P exceed 2^32.
                     load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
-                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), -m, pk);
-                    slow = !__all_sync(0xffffffffu, rowsum <= 18446744073709551616.f);
-                }
-                if (slow) {
-                    load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
-                    const float m_tile = row_max(x) * scale_log2;
-                    m_new = m_tile > m ? m_tile : m;
-                    alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
-                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), m_new == -INFINITY ? 0.f : -m_new, pk);
-                }
-                const bool rescale = (m_new != m) && j > 0;
-                if (C::SEP_P) {
-                    // S_t(j) is no longer needed: the MMA warp may compute S_t(j+1) now
                     tc_fence_before();
                     mbar_arrive(bar_sfree + 8u * t);
+                    const float m_tile = row_max(x) * scale_log2;
+                    if (m_tile > m + 32.0f) m_new = m_tile;
+                    alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), m_new == -INFINITY ? 0.f : -m_new, pk);
+                } else {
+                    // P overwrites S in place, so S_t(j) stays readable until P is written.
+                    // Fast path (every key tile after the first): no row maximum.  P is computed
+                    // against the current reference m; any reference gives the same O / l, it
+                    // only has to keep P finite.  If some row's sum exceeds 2^64 (or is not
+                    // finite) the warp redoes the tile with the exact maximum (slow path, also
+                    // used for j = 0).
+                    bool slow = j == 0;
+                    if (!slow) {
+                        load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
+                        rowsum = exp_tile(x, pack2(scale_log2, scale_log2), -m, pk);
+                        slow = !__all_sync(0xffffffffu, rowsum <= 18446744073709551616.f);
+                    }
+                    if (slow) {
+                        load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
+                        const float m_tile = row_max(x) * scale_log2;
+                        m_new = m_tile > m ? m_tile : m;
+                        alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+                        rowsum = exp_tile(x, pack2(scale_log2, scale_log2),
+                                          m_new == -INFINITY ? 0.f : -m_new, pk);
+                    }
                 }
+                const bool rescale = (m_new != m) && j > 0;
                 if (C::SEP_P && j > 0) {
                     // PV_t(j-1) done: O_t is stable and the P_t columns are free
                     if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone + 8u * t, (uint32_t)(j - 1) & 1u,

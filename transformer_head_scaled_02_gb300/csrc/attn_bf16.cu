@@ -27,9 +27,9 @@
 // Warp roles (384 threads):
 //   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a ring of stages;
 //   warp 1      TMEM owner and MMA issuer.  Per key tile j:
-//                 d = 64:  warps 1 and 2 each issue for one query tile t: S_t(j+1) as soon
-//                          as the softmax has read S_t(j), then O_t += P_t V_j as soon as
-//                          P_t is in TMEM;
+//                 d = 64:  warp 1 issues the score MMAs S_t(j+1) (as soon as the softmax
+//                          has read S_t(j)), warp 2 the PV MMAs O_t += P_t V_j (as soon as P_t
+//                          is in TMEM), for both query tiles;
 //                 d = 128: warp 1 alone, alternating the tiles:
 //                          O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j, S_1(j+1)
 //               (tcgen05 MMAs of one thread execute in issue order, so S_t may overwrite the
@@ -68,9 +68,9 @@ struct AttnCfg {
     static constexpr int SMEM = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + BAR_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr bool SEP_P = HD == 64;  // P in its own TMEM columns
-    // MMA-issuing threads: one per query tile when P has its own columns (the tiles' chains
-    // are independent); one for both tiles when P lives in S, where strict alternation
-    // between the tiles keeps the two softmax groups out of phase.
+    // MMA-issuing threads: with P in its own columns, one for the score MMAs and one for the
+    // PV MMAs (independent chains); with P inside S, one for everything, strictly alternating
+    // the tiles, which keeps the two softmax groups out of phase.
     static constexpr int ISSUERS = SEP_P ? 2 : 1;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return (uint32_t)(128 * t); }
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return (uint32_t)(256 + HD * t); }
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_kfull + 8u * s, 1);
             mbar_init(bar_vfull + 8u * s, 1);
-            mbar_init(bar_kvempty + 8u * s, C::ISSUERS);  // one commit per MMA-issuing thread
+            mbar_init(bar_kvempty + 8u * s, 1);  // committed by the thread issuing the PV MMAs
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_sfull + 8u * t, 1);
@@ -307,84 +307,68 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         }
     } else if (C::ISSUERS == 2 && (warp == 1 || warp == 2)) {
         if (lane == 0) {
-            // ---------------- MMA issuers: warp 1 for query tile 0, warp 2 for tile 1.
-            // tcgen05.mma issue is paced by the tensor core (the issuing thread stalls while
-            // its queue is full), so every wait/commit between MMA batches of one thread is
-            // a bubble; with one issuing thread per tile, one thread's waits overlap the
-            // other's MMAs.  The tiles are independent (own TMEM columns); both threads read
-            // the same K/V stages and each commits once per key tile to release a stage.
-            const int t = warp - 1;
-            const int n = n_t[t];
-            // Descriptors are built once; per MMA only the start-address field changes, by
-            // adding the (16-byte granular) offset of the K step to the stage's descriptor.
+            // ---------------- MMA issuers for d = 64: warp 1 issues every score MMA, warp 2
+            // every PV MMA, both query tiles.  tcgen05.mma issue is paced by the tensor core
+            // (the issuing thread stalls while its queue is full), so one thread's waits would
+            // idle the tensor core; and with P in its own TMEM columns the two chains are
+            // independent: S_t(j+1) needs only the softmax's read of S_t(j), PV_t(j) only P_t(j).
+            // Per query tile the MMAs still execute in issue order within each chain.
             const uint32_t idesc_s = idesc_bf16_f32(128, C::BN, false, false);
             const uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
             const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
             const uint64_t vdesc0 = sdesc_sw128(sV, C::CHUNK, 1024);
-            const uint64_t qdesc = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
-            // S_t = Q_t K_j^T into S_t's columns, then signal s_full_t
-            auto issue_s = [&](int j) {
-                const uint64_t kdesc = kdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
-                    mma_bf16_ss(tmem_base + C::S_COL(t), qdesc + off16, kdesc + off16, idesc_s,
-                                kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar_sfull + 8u * t);
-            };
-            // O_t += P_t V_j, then signal pv_done_t
-            auto issue_pv = [&](int j) {
-                const uint64_t vdesc = vdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::P_COL(t) + kk * 8,
-                                vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar_pvdone + 8u * t);
-            };
-            auto wait_k = [&](int j) {
-                return mbar_wait(bar_kfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
-            };
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
             bool ok = true;
-            if (n > 0) {
-                ok = mbar_wait(bar_q, 0, abort_flag, status) && wait_k(0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                }
-            }
-            int j = 0;
-            for (; j < n && ok; ++j) {
-                const int jn = j + 1;
-                if (C::SEP_P && jn < n) {
-                    // next scores first: only the softmax's read of S_t(j) gates them
-                    ok = wait_k(jn) &&
-                         mbar_wait(bar_sfree + 8u * t, (uint32_t)j & 1u, abort_flag, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(jn);
-                }
-                ok = mbar_wait(bar_vfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status) &&
-                     mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(j);
-                if (!C::SEP_P && jn < n) {
-                    // P_t lives in S_t's columns: S_t(j+1) goes after the PV that reads P_t(j)
-                    if (!wait_k(jn)) {
-                        ok = false;
-                        break;
+            if (warp == 1) {
+                // scores: S_t(j) = Q_t K_j^T, signalled on s_full_t
+                auto issue_s = [&](int t, int j) {
+                    const uint64_t kdesc = kdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
+                    const uint64_t qdesc = qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
+                        mma_bf16_ss(tmem_base + C::S_COL(t), qdesc + off16, kdesc + off16, idesc_s,
+                                    kk > 0 ? 1u : 0u);
                     }
-                    tc_fence_after();
-                    issue_s(jn);
+                    tc_commit(bar_sfull + 8u * t);
+                };
+                for (int j = 0; j < n_max && ok; ++j) {
+                    ok = (j == 0 ? mbar_wait(bar_q, 0, abort_flag, status) : true) &&
+                         mbar_wait(bar_kfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
+#pragma unroll
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        // S_t(j) may overwrite S_t only once the softmax has read S_t(j-1)
+                        if (j > 0)
+                            ok = mbar_wait(bar_sfree + 8u * t, (uint32_t)(j - 1) & 1u, abort_flag, status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(t, j);
+                    }
                 }
-                tc_commit(bar_kvempty + 8u * (j % S));
+            } else {
+                // weighted sums: O_t += P_t V_j, signalled on pv_done_t; then the stage of key
+                // tile j is released (the score MMAs that read K_j completed before P_t(j) could
+                // be written)
+                for (int j = 0; j < n_max && ok; ++j) {
+                    ok = mbar_wait(bar_vfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
+                    const uint64_t vdesc = vdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
+#pragma unroll
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        ok = mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < C::BN / 16; ++kk)
+                            mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::P_COL(t) + kk * 8,
+                                        vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar_pvdone + 8u * t);
+                    }
+                    if (ok) tc_commit(bar_kvempty + 8u * (j % S));
+                }
             }
-            // release the stages of key tiles this query tile does not use (the other tile
-            // may need one more key tile under the causal mask)
-            if (ok)
-                for (; j < n_max; ++j) tc_commit(bar_kvempty + 8u * (j % S));
             tc_commit(bar_drain);
             drain_wait_a(bar_drain, 0);
         }

@@ -589,6 +589,465 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// d = 64: persistent CTAs, two per SM, one 128-row query tile at a time.
+//
+// With d = 64 a 128x128 key tile costs the tensor core 2 x 256 cycles per query tile and the
+// softmax 16384 exponentials, which the MUFU retires at 32 per clock per SM at best, so the
+// softmax must never wait.  Two CTAs per SM (256 TMEM columns each: S 128, O 64, P 64; 96 KB
+// of shared memory) advance independently, so one CTA's softmax keeps the MUFU busy while the
+// other reads S or stores P.  Each CTA is persistent: it walks a list of work items (one
+// query tile of one (batch, head)), and the start of item i+1 -- its Q tile, its first K/V
+// tiles and its first score MMA -- overlaps the end of item i (last softmax, last PV product,
+// output store), which would otherwise leave the SM idle for thousands of cycles per item.
+//
+// Work items are numbered longest first (causal: the last query tiles of every head first)
+// and dealt to the CTAs in a snake order (0..G-1, then G-1..0, ...), which balances the
+// causal triangle across CTAs.
+//
+// Warp roles (256 threads; warps 0-3 run on 56 registers, the softmax warps on 200):
+//   warp 0      TMA: per item the Q tile into one of two Q buffers (once the output of the
+//               item two back has left it), then the K tiles through a ring of DK_STAGES
+//               (freed when the score MMA that read them completes);
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T for the next key tile (of this item or
+//               the next) as soon as the softmax has read the current S, then O += P V as
+//               soon as P is in TMEM;
+//   warp 2      TMA: the V tiles through a ring of DV_STAGES (freed when the PV MMA completes);
+//   warp 3      TMA: stores each item's output, which the softmax leaves in the item's Q buffer;
+//   warps 4-7   softmax, one query row per thread (TMEM lane quarter = warp & 3).
+constexpr int DK_STAGES = 2;
+constexpr int DV_STAGES = 2;
+constexpr int D64_THREADS = 256;
+constexpr int D64_REGS_CTRL = 56;
+constexpr int D64_REGS_SOFTMAX = 200;
+constexpr int D64_TILE = 128 * 128;  // one 128-row x 64-column bf16 box, 16 KB
+constexpr int D64_BAR_BYTES = 256;
+constexpr int D64_SMEM = D64_TILE * (2 + DK_STAGES + DV_STAGES) + D64_BAR_BYTES + 1024;
+// two CTAs (each with its 1 KB of reserved shared memory) must fit one SM's 228 KB
+static_assert(2 * (D64_SMEM + 1024) <= 233472, "two d=64 CTAs per SM");
+// the register split must fit the 128 registers per thread two CTAs are launched with
+static_assert(128 * D64_REGS_CTRL + 128 * D64_REGS_SOFTMAX <= D64_THREADS * 128, "register split");
+constexpr uint32_t D64_TMEM_COLS = 256;
+constexpr uint32_t D64_S_COL = 0, D64_O_COL = 128, D64_P_COL = 192;
+
+struct D64Item {
+    int b, head, qrow0, n;  // n = key tiles to visit (0: no valid key)
+    bool bad;
+};
+
+// Item k of the longest-first numbering.
+__device__ __forceinline__ D64Item d64_item(int k, int BH, int h, int n_qt, int causal,
+                                            const int32_t* kv_lengths, int T_kv) {
+    D64Item it;
+    const int rank = k / BH;
+    const int bh = k - rank * BH;
+    const int qt = causal ? n_qt - 1 - rank : rank;
+    it.b = bh / h;
+    it.head = bh - it.b * h;
+    it.qrow0 = qt * 128;
+    const int L = kv_lengths != nullptr ? kv_lengths[it.b] : T_kv;
+    it.bad = L < 1 || L > T_kv;
+    int n = (L + 127) / 128;
+    if (causal) n = n < qt + 1 ? n : qt + 1;  // key tiles up to the diagonal
+    it.n = it.bad ? 0 : n;
+    return it;
+}
+
+// The r-th item of CTA c among G CTAs (snake order).
+__device__ __forceinline__ int d64_item_index(int r, int G, int c) {
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
+__global__ void __launch_bounds__(D64_THREADS, 2)
+    attn_bf16_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO, int B, int h, int T_q, int T_kv,
+                         int causal, const int32_t* __restrict__ kv_lengths, float scale_log2,
+                         int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sQ = base;  // two Q buffers; item r uses buffer r & 1, also for its output
+    const uint32_t sK = sQ + 2 * D64_TILE;
+    const uint32_t sV = sK + DK_STAGES * D64_TILE;
+    const uint32_t sBar = sV + DV_STAGES * D64_TILE;
+    // barriers: q_full[2], staged[2], q_free[2], k_full[DK], k_empty[DK], v_full[DV],
+    //           v_empty[DV], s_full, s_free, p_full, pv_done, mma_drain
+    const uint32_t bar_qfull = sBar;
+    const uint32_t bar_staged = bar_qfull + 16u;
+    const uint32_t bar_qfree = bar_staged + 16u;
+    const uint32_t bar_kfull = bar_qfree + 16u;
+    const uint32_t bar_kempty = bar_kfull + 8u * DK_STAGES;
+    const uint32_t bar_vfull = bar_kempty + 8u * DK_STAGES;
+    const uint32_t bar_vempty = bar_vfull + 8u * DV_STAGES;
+    const uint32_t bar_sfull = bar_vempty + 8u * DV_STAGES;
+    const uint32_t bar_sfree = bar_sfull + 8u;
+    const uint32_t bar_pfull = bar_sfree + 8u;
+    const uint32_t bar_pvdone = bar_pfull + 8u;
+    const uint32_t bar_drain = bar_pvdone + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int BH = B * h;
+    const int n_qt = (T_q + 127) / 128;
+    const int N = BH * n_qt;
+    const int G = (int)gridDim.x;
+    const int c = (int)blockIdx.x;
+    int R = 0;  // items of this CTA
+    while (d64_item_index(R, G, c) < N) ++R;
+    auto item = [&](int r) {
+        return d64_item(d64_item_index(r, G, c), BH, h, n_qt, causal, kv_lengths, T_kv);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_qfull + 8u * i, 1);
+            mbar_init(bar_staged + 8u * i, 128);
+            mbar_init(bar_qfree + 8u * i, 1);
+        }
+        for (int s = 0; s < DK_STAGES; ++s) {
+            mbar_init(bar_kfull + 8u * s, 1);
+            mbar_init(bar_kempty + 8u * s, 1);
+        }
+        for (int s = 0; s < DV_STAGES; ++s) {
+            mbar_init(bar_vfull + 8u * s, 1);
+            mbar_init(bar_vempty + 8u * s, 1);
+        }
+        mbar_init(bar_sfull, 1);
+        mbar_init(bar_sfree, 128);
+        mbar_init(bar_pfull, 128);
+        mbar_init(bar_pvdone, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), D64_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < 4) {
+      setmaxnreg_dec<D64_REGS_CTRL>();
+      if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA: Q and K
+            tma_prefetch_desc(&tmK);
+            uint32_t gk = 0;  // K tiles issued
+            int rq = -1;      // last item whose Q load was issued
+            bool ok = true;
+            for (int r = 0; r < R && ok; ++r) {
+                const D64Item it = item(r);
+                // the Q buffer of item r held the output of item r-2 until it was stored
+                if (r >= 2 && !mbar_wait(bar_qfree + 8u * (r & 1), (uint32_t)((r - 2) >> 1) & 1u,
+                                         abort_flag, status))
+                    break;
+                if (it.bad) record_status(status, kStatusBadLength);
+                const uint32_t qb = bar_qfull + 8u * (r & 1);
+                mbar_arrive_expect_tx(qb, D64_TILE);
+                tma_load_3d(sQ + (uint32_t)(r & 1) * D64_TILE, &tmQ, it.head * 64, it.qrow0, it.b, qb);
+                rq = r;
+                for (int j = 0; j < it.n; ++j) {
+                    const uint32_t st = gk % DK_STAGES;
+                    ok = mbar_wait(bar_kempty + 8u * st, ((gk / DK_STAGES) & 1u) ^ 1u, abort_flag, status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar_kfull + 8u * st, D64_TILE);
+                    tma_load_3d(sK + st * D64_TILE, &tmK, it.head * 64, j * 128, it.b, bar_kfull + 8u * st);
+                    ++gk;
+                }
+            }
+            // every load issued lands before the CTA exits
+            for (uint32_t g = gk > DK_STAGES ? gk - DK_STAGES : 0; g < gk; ++g)
+                drain_wait_a(bar_kfull + 8u * (g % DK_STAGES), (g / DK_STAGES) & 1u);
+            for (int r = rq > 1 ? rq - 1 : 0; r <= rq; ++r)
+                drain_wait_a(bar_qfull + 8u * (r & 1), (uint32_t)(r >> 1) & 1u);
+        }
+      } else if (warp == 2) {
+        if (lane == 0) {
+            // ---------------- TMA: V
+            tma_prefetch_desc(&tmV);
+            uint32_t gv = 0;  // V tiles issued
+            bool ok = true;
+            for (int r = 0; r < R && ok; ++r) {
+                const D64Item it = item(r);
+                for (int j = 0; j < it.n; ++j) {
+                    const uint32_t st = gv % DV_STAGES;
+                    ok = mbar_wait(bar_vempty + 8u * st, ((gv / DV_STAGES) & 1u) ^ 1u, abort_flag, status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar_vfull + 8u * st, D64_TILE);
+                    tma_load_3d(sV + st * D64_TILE, &tmV, it.head * 64, j * 128, it.b, bar_vfull + 8u * st);
+                    ++gv;
+                }
+            }
+            for (uint32_t g = gv > DV_STAGES ? gv - DV_STAGES : 0; g < gv; ++g)
+                drain_wait_a(bar_vfull + 8u * (g % DV_STAGES), (g / DV_STAGES) & 1u);
+        }
+      } else if (warp == 3) {
+        if (lane == 0) {
+            // ---------------- TMA: outputs, each as soon as the softmax has staged it
+            for (int r = 0; r < R; ++r) {
+                if (!mbar_wait(bar_staged + 8u * (r & 1), (uint32_t)(r >> 1) & 1u, abort_flag, status))
+                    break;
+                const D64Item it = item(r);
+                if (!*abort_flag && it.qrow0 < T_q) {
+                    tma_store_3d(&tmO, sQ + (uint32_t)(r & 1) * D64_TILE, it.head * 64, it.qrow0, it.b);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                }
+                mbar_arrive(bar_qfree + 8u * (r & 1));
+            }
+            bulk_wait_group<0>();
+        }
+      } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t idesc_o = idesc_bf16_f32(128, 64, false, true);
+            const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t vdesc0 = sdesc_sw128(sV, D64_TILE, 1024);
+            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+            uint32_t gk = 0, gv = 0, gs = 0, gp = 0;  // K, V consumed; S, PV issued
+            bool ok = true;
+            // S = Q_r K^T for the next K tile, once the softmax has read the previous S
+            auto issue_s = [&](int r) -> bool {
+                const uint32_t st = gk % DK_STAGES;
+                if (!mbar_wait(bar_kfull + 8u * st, (gk / DK_STAGES) & 1u, abort_flag, status)) return false;
+                if (gs > 0 && !mbar_wait(bar_sfree, (gs - 1) & 1u, abort_flag, status)) return false;
+                tc_fence_after();
+                const uint64_t kdesc = kdesc0 + (uint64_t)((st * D64_TILE) >> 4);
+                const uint64_t qdesc = qdesc0 + (uint64_t)(((uint32_t)(r & 1) * D64_TILE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem_base + D64_S_COL, qdesc + (uint64_t)(kk * 2),
+                                kdesc + (uint64_t)(kk * 2), idesc_s, kk > 0 ? 1u : 0u);
+                tc_commit(bar_sfull);
+                tc_commit(bar_kempty + 8u * st);
+                ++gk;
+                ++gs;
+                return true;
+            };
+            // the first score MMA of item r (an item without keys has none; its Q load is
+            // waited for by the softmax instead)
+            auto start_item = [&](int r, const D64Item& it) -> bool {
+                if (it.n == 0) return true;
+                if (!mbar_wait(bar_qfull + 8u * (r & 1), (uint32_t)(r >> 1) & 1u, abort_flag, status))
+                    return false;
+                return issue_s(r);
+            };
+            D64Item cur = item(0);
+            ok = start_item(0, cur);
+            for (int r = 0; r < R && ok; ++r) {
+                D64Item nxt;
+                nxt.n = 0;
+                if (r + 1 < R) nxt = item(r + 1);
+                if (cur.n == 0 && r + 1 < R) ok = start_item(r + 1, nxt);
+                for (int j = 0; j < cur.n && ok; ++j) {
+                    if (j + 1 < cur.n)
+                        ok = issue_s(r);
+                    else if (r + 1 < R)
+                        ok = start_item(r + 1, nxt);
+                    if (!ok) break;
+                    const uint32_t st = gv % DV_STAGES;
+                    ok = mbar_wait(bar_vfull + 8u * st, (gv / DV_STAGES) & 1u, abort_flag, status) &&
+                         mbar_wait(bar_pfull, gp & 1u, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t vdesc = vdesc0 + (uint64_t)((st * D64_TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ts(tmem_base + D64_O_COL, tmem_base + D64_P_COL + kk * 8,
+                                    vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_pvdone);
+                    tc_commit(bar_vempty + 8u * st);
+                    ++gv;
+                    ++gp;
+                }
+                cur = nxt;
+            }
+            tc_commit(bar_drain);
+            drain_wait_a(bar_drain, 0);
+        }
+      }
+    } else {
+        setmaxnreg_inc<D64_REGS_SOFTMAX>();
+        // ---------------- softmax: thread = query row
+        const int q = warp & 3;
+        const int r_ = q * 32 + lane;
+        const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+        const uint32_t sw = (uint32_t)(r_ & 7);
+        uint32_t gs = 0, gp = 0;  // S read, P written
+        bool ok = true;
+        for (int r = 0; r < R && ok; ++r) {
+            const D64Item it = item(r);
+            const uint32_t sOut = sQ + (uint32_t)(r & 1) * D64_TILE;
+            const int row = it.qrow0 + r_;
+            if (it.n == 0) {
+                // no valid key: the softmax is undefined, the rows are NaN (written once the
+                // item's Q load, which targets the same buffer, has landed)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_qfull + 8u * (r & 1), (uint32_t)(r >> 1) & 1u,
+                                                       abort_flag, status));
+                if (!ok) break;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(sOut + r_ * 128 + ((u ^ sw) << 4), 0x7FC07FC0u, 0x7FC07FC0u,
+                                 0x7FC07FC0u, 0x7FC07FC0u);
+            } else {
+                float m = -INFINITY;  // reference maximum, already scaled to base 2
+                float l = 0.f;
+                const int L = kv_lengths != nullptr ? kv_lengths[it.b] : T_kv;
+                for (int j = 0; j < it.n && ok; ++j) {
+                    // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, gs & 1u, abort_flag, status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int kv0 = j * 128;
+                    const bool masked = kv0 + 128 > L || (causal && kv0 + 127 > it.qrow0);
+                    const int lim = causal ? min(L, row + 1) : L;  // keys [0, lim) are visible
+                    float x[128];
+                    load_s_tile(trow + D64_S_COL, masked, kv0, lim, x);
+                    tc_fence_before();
+                    mbar_arrive(bar_sfree);
+                    ++gs;
+                    // the reference moves only when it would otherwise let P exceed 2^32
+                    const float m_tile = row_max(x) * scale_log2;
+                    const float m_new = m_tile > m + 32.0f ? m_tile : m;
+                    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+                    uint32_t pk[64];
+                    const float rowsum = exp_tile(x, pack2(scale_log2, scale_log2),
+                                                  m_new == -INFINITY ? 0.f : -m_new, pk);
+                    if (j > 0) {
+                        // the previous PV product is done: O is stable and the P columns are free
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone, (gp - 1) & 1u, abort_flag, status))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const bool rescale = (m_new != m) && j > 0;
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        const float a = rescale ? alpha : 1.f;
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            uint32_t o[32];
+                            tmem_ld32(trow + D64_O_COL + cc * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                            tmem_st32(trow + D64_O_COL + cc * 32, o);
+                        }
+                    }
+                    {
+                        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+                        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+                        tmem_st32(trow + D64_P_COL, p0);
+                        tmem_st32(trow + D64_P_COL + 32, p1);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar_pfull);
+                    ++gp;
+                    l = l * alpha + rowsum;
+                    m = m_new;
+                }
+                if (!ok || !__all_sync(0xffffffffu, mbar_wait(bar_pvdone, (gp - 1) & 1u, abort_flag, status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float inv = 1.f / l;
+                // O / l as bf16 into the item's Q buffer (its last score MMA has completed)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(trow + D64_O_COL + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const int u = cc * 4 + u4;
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
+                        st_shared_v4(sOut + r_ * 128 + (((uint32_t)u ^ sw) << 4),
+                                     pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                }
+                // the next item's PV product overwrites O: the reads above must be complete
+                tc_fence_before();
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_staged + 8u * (r & 1));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, D64_TMEM_COLS);
+    }
+}
+
+cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t ldk,
+                            const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
+                            int T_q, int T_kv, int causal, const int32_t* kv_lengths, int num_sms,
+                            int* status, cudaStream_t stream) {
+    CUtensorMap tQ, tK, tV, tO;
+    const uint32_t box[3] = {64, 128, 1};
+    {
+        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_q, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)ldq * 2, (uint64_t)ldq * 2 * (uint64_t)T_q};
+        if (!encode_tmap_bf16(&tQ, Q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)ldk * 2, (uint64_t)ldk * 2 * (uint64_t)T_kv};
+        if (!encode_tmap_bf16(&tK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)ldv * 2, (uint64_t)ldv * 2 * (uint64_t)T_kv};
+        if (!encode_tmap_bf16(&tV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_q, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)ldo * 2, (uint64_t)ldo * 2 * (uint64_t)T_q};
+        if (!encode_tmap_bf16(&tO, O, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    // setmaxnreg.inc waits until the CTA's register pool (threads x registers at launch) can
+    // grant the rise: refuse to launch a build whose register count cannot cover the split
+    static int pool_ok = -1;
+    if (pool_ok < 0) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, attn_bf16_d64_kernel);
+        if (e != cudaSuccess) return e;
+        pool_ok = fa.numRegs * D64_THREADS >= 128 * (D64_REGS_CTRL + D64_REGS_SOFTMAX) ? 1 : 0;
+    }
+    if (!pool_ok) return cudaErrorInvalidConfiguration;
+    cudaError_t err = cudaFuncSetAttribute(attn_bf16_d64_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, D64_SMEM);
+    if (err != cudaSuccess) return err;
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt(64.0));
+    const int64_t items = (int64_t)B * h * ((T_q + 127) / 128);
+    if (items > INT32_MAX) return cudaErrorInvalidValue;
+    const int64_t slots = 2 * (int64_t)(num_sms > 0 ? num_sms : 1);
+    const int grid = (int)(items < slots ? items : slots);
+    attn_bf16_d64_kernel<<<grid, D64_THREADS, D64_SMEM, stream>>>(tQ, tK, tV, tO, B, h, T_q, T_kv,
+                                                                  causal, kv_lengths, scale_log2, status);
+    return cudaGetLastError();
+}
+
 template <int HD>
 cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ldk, const void* V,
                            int64_t ldv, void* O, int64_t ldo, int B, int h, int T_q, int T_kv,
@@ -633,10 +1092,10 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
 cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t ldk,
                              const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
                              int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
-                             int* status, cudaStream_t stream) {
+                             int num_sms, int* status, cudaStream_t stream) {
     if (d == 64)
-        return launch_attn_hd<64>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
-                                  kv_lengths, status, stream);
+        return launch_attn_d64(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
+                               kv_lengths, num_sms, status, stream);
     if (d == 128)
         return launch_attn_hd<128>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
                                    kv_lengths, status, stream);

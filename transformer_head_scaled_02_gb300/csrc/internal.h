@@ -42,10 +42,11 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
                              const void* bias, void* C, int64_t ldc, int M, int N, int K,
                              int num_sms, int* status, cudaStream_t stream);
 
-// Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v).
+// Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v).  num_sms sizes the
+// persistent grid of the d = 64 kernel.
 cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t ldk,
                              const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
                              int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
-                             int* status, cudaStream_t stream);
+                             int num_sms, int* status, cudaStream_t stream);
 
 }  // namespace mha

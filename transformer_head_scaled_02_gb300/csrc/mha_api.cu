@@ -154,8 +154,11 @@ mha_status run_attention(const mha_s* m, int B, int T_q, int T_kv, const void* Q
                                    ldo, B, m->h, T_q, T_kv, m->dk, m->dv, causal, kv_lengths,
                                    status_ptr(m), stream);
     } else {
+        int sms = 0;
+        const mha_status st = query_sms(&sms);
+        if (st != MHA_OK) return st;
         err = mha::launch_attn_bf16(Q, ldq, K, ldk, V, ldv, O, ldo, B, m->h, T_q, T_kv, m->dk,
-                                    causal, kv_lengths, status_ptr(m), stream);
+                                    causal, kv_lengths, sms, status_ptr(m), stream);
     }
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -172,6 +175,7 @@ mha_status check_attention_shape(const mha_s* m, int B, int T_q, int T_kv, int c
     } else {
         if (!bf16_shape_supported(m)) return MHA_ERR_UNSUPPORTED;
         if ((T_q + 127) / 128 > 65535) return MHA_ERR_UNSUPPORTED;
+        if ((int64_t)B * m->h * ((T_q + 127) / 128) > INT32_MAX) return MHA_ERR_UNSUPPORTED;
     }
     return MHA_OK;
 }

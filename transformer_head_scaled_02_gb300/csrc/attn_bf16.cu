@@ -1093,9 +1093,18 @@ cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t 
                              const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
                              int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
                              int num_sms, int* status, cudaStream_t stream) {
-    if (d == 64)
+    // d = 64: causal self-attention without key lengths (query tiles of a head differ only in
+    // their causal length, and the lengths are known here) runs on the persistent kernel,
+    // whose fixed item order balances them; with key lengths (known only on the device) or
+    // without the causal mask, every item is long and the CTA-per-tile-pair kernel, whose
+    // two query tiles share each K/V tile and whose CTAs the hardware schedules as they
+    // finish, is the better fit
+    if (d == 64 && causal && kv_lengths == nullptr)
         return launch_attn_d64(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
                                kv_lengths, num_sms, status, stream);
+    if (d == 64)
+        return launch_attn_hd<64>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
+                                  kv_lengths, status, stream);
     if (d == 128)
         return launch_attn_hd<128>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
                                    kv_lengths, status, stream);

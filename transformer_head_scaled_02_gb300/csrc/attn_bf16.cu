@@ -224,21 +224,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int qb = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
     const int q0 = qb * (C::NQ * C::BM);
 
-    const int L = kv_lengths != nullptr ? kv_lengths[b] : T_kv;
-    const bool bad = L < 1 || L > T_kv;
-    const int nL = (L + C::BN - 1) / C::BN;
-    int n_t[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        int n = nL;
-        if (causal) {
-            const int nc = (q0 + C::BM * t + C::BM + C::BN - 1) / C::BN;  // key tiles up to the diagonal
-            n = n < nc ? n : nc;
-        }
-        n_t[t] = bad ? 0 : n;
-    }
-    const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
-
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < S; ++s) {
@@ -255,7 +240,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         mbar_init(bar_drain, C::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
-        if (bad) record_status(status, kStatusBadLength);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -265,6 +249,25 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Q, K, V and the key lengths may come from the previous kernel on the stream
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int L = kv_lengths != nullptr ? kv_lengths[b] : T_kv;
+    const bool bad = L < 1 || L > T_kv;
+    const int nL = (L + C::BN - 1) / C::BN;
+    int n_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        int n = nL;
+        if (causal) {
+            const int nc = (q0 + C::BM * t + C::BM + C::BN - 1) / C::BN;  // key tiles up to the diagonal
+            n = n < nc ? n : nc;
+        }
+        n_t[t] = bad ? 0 : n;
+    }
+    const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
+    if (threadIdx.x == 0 && bad) record_status(status, kStatusBadLength);
 
     if (warp == 0) {
         if (lane == 0 && n_max > 0) {
@@ -734,6 +737,9 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Q, K, V and the key lengths may come from the previous kernel on the stream
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp < 4) {
       setmaxnreg_dec<D64_REGS_CTRL>();
@@ -1043,9 +1049,8 @@ cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t l
     if (items > INT32_MAX) return cudaErrorInvalidValue;
     const int64_t slots = 2 * (int64_t)(num_sms > 0 ? num_sms : 1);
     const int grid = (int)(items < slots ? items : slots);
-    attn_bf16_d64_kernel<<<grid, D64_THREADS, D64_SMEM, stream>>>(tQ, tK, tV, tO, B, h, T_q, T_kv,
-                                                                  causal, kv_lengths, scale_log2, status);
-    return cudaGetLastError();
+    return launch_pdl(attn_bf16_d64_kernel, dim3(grid), dim3(D64_THREADS), D64_SMEM, stream, tQ, tK, tV,
+                      tO, B, h, T_q, T_kv, causal, kv_lengths, scale_log2, status);
 }
 
 template <int HD>
@@ -1082,9 +1087,8 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     const int rows_per_cta = C::NQ * C::BM;
     const dim3 grid((unsigned)(B * h), (unsigned)((T_q + rows_per_cta - 1) / rows_per_cta));
-    attn_bf16_tc_kernel<HD><<<grid, A_THREADS, C::SMEM, stream>>>(tQ, tK, tV, tO, h, T_q, T_kv, causal,
-                                                                   kv_lengths, scale_log2, status);
-    return cudaGetLastError();
+    return launch_pdl(attn_bf16_tc_kernel<HD>, grid, dim3(A_THREADS), C::SMEM, stream, tQ, tK, tV, tO,
+                      h, T_q, T_kv, causal, kv_lengths, scale_log2, status);
 }
 
 }  // namespace

@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // inputs may come from the previous kernel on the stream
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -339,6 +342,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // inputs may come from the previous kernel on the stream
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -557,17 +563,15 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         }
         const int pair_tiles = ((M + 255) / 256) * ((N + G_BN - 1) / G_BN);
         const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-        gemm_bf16_pair_kernel<<<2 * pairs, G_THREADS, P_SMEM, stream>>>(
-            tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
-        return cudaGetLastError();
+        return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream,
+                          tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
     }
     cudaError_t err = cudaFuncSetAttribute(gemm_bf16_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (err != cudaSuccess) return err;
     const int grid = num_tiles < num_sms ? num_tiles : num_sms;
-    gemm_bf16_tc_kernel<<<grid, G_THREADS, G_SMEM, stream>>>(
-        tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
-    return cudaGetLastError();
+    return launch_pdl(gemm_bf16_tc_kernel, dim3(grid), dim3(G_THREADS), G_SMEM, stream, tA, tW, tC,
+                      reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
 }
 
 }  // namespace mha

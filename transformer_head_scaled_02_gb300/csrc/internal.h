@@ -19,6 +19,27 @@ struct mha_s {
 
 namespace mha {
 
+// Launch a kernel that may start while the previous kernel on the stream is finishing
+// (programmatic dependent launch): its CTAs run their set-up (barriers, TMEM allocation)
+// early and wait in grid_dependency_wait() until the previous grid has completed and its
+// memory is visible.  Every kernel launched this way calls grid_dependency_wait() before
+// its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Encode a bf16 tiled tensor map with 128-byte swizzle and zero fill out of bounds.
 // dims[0] is the innermost (contiguous) extent; strides_bytes has rank-1 entries.
 // Returns false if the driver entry point is unavailable or rejects the map.

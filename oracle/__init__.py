@@ -77,6 +77,25 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _dp, _dp, _dp, _dp, _dp, _dp,
                 ctypes.c_int, _ip, _ip, ctypes.c_int, _dp, ctypes.c_int]
+            lib.oracle_attention_grouped.restype = ctypes.c_int
+            lib.oracle_attention_grouped.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int,
+                _dp, ctypes.c_long, _dp, ctypes.c_long, _dp, ctypes.c_long,
+                ctypes.c_int, _ip, _ip, ctypes.c_int, _dp, ctypes.c_long, _dp,
+                ctypes.c_int]
+            lib.oracle_mha_forward_ex.restype = ctypes.c_int
+            lib.oracle_mha_forward_ex.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                ctypes.c_int, _ip, _ip, ctypes.c_int, _dp, ctypes.c_int]
+            lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int,
+                _dp, ctypes.c_long, _dp, ctypes.c_long, _dp, ctypes.c_long,
+                _ip, _dp, ctypes.c_long, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -126,38 +145,52 @@ def linear(X, W, b=None, nthreads: int = 0):
 
 
 def attention(Q, K, V, h: int, causal: bool = False, kv_lengths=None, rows=None,
-              return_weights: bool = False, nthreads: int = 0):
+              return_weights: bool = False, nthreads: int = 0, h_kv=None):
     """Attention of every head over already-projected Q (B,Tq,h*dk),
-    K (B,Tkv,h*dk), V (B,Tkv,h*dv).  Returns Ocat (B, n_out, h*dv) -- the
-    Concat of the heads -- and, if asked, the weights (B, h, n_out, Tkv)."""
+    K (B,Tkv,h_kv*dk), V (B,Tkv,h_kv*dv) (h_kv = h unless given: grouped K/V heads,
+    query head i using K/V head i // (h // h_kv)).  Returns Ocat (B, n_out, h*dv) --
+    the Concat of the heads -- and, if asked, the weights (B, h, n_out, Tkv)."""
     lib = _load()
     Q = _f64(Q)
     K = _f64(K)
     V = _f64(V)
+    h_kv = h if h_kv is None else int(h_kv)
     B, Tq, hdk = Q.shape
-    _, Tkv, hdv = V.shape
-    if hdk % h or hdv % h:
-        raise ValueError("head count does not divide the projection widths")
-    dk, dv = hdk // h, hdv // h
+    _, Tkv, kvw = V.shape
+    if hdk % h or kvw % h_kv or h % h_kv:
+        raise ValueError("head counts do not divide the projection widths")
+    dk, dv = hdk // h, kvw // h_kv
+    if K.shape[2] != h_kv * dk:
+        raise ValueError("K width is not h_kv * d_k")
+    hdv = h * dv
     kvl = _i32(kv_lengths)
     rws = _i32(rows)
     n_out = Tq if rws is None else len(rws)
     O = np.empty((B, n_out, hdv), dtype=np.float64)
     P = np.empty((B, h, n_out, Tkv), dtype=np.float64) if return_weights else None
-    rc = lib.oracle_attention(B, Tq, Tkv, h, dk, dv, _ptr(Q), hdk, _ptr(K), hdk, _ptr(V), hdv,
-                              int(bool(causal)), _iptr(kvl), _iptr(rws),
-                              0 if rws is None else len(rws), _ptr(O), hdv, _ptr(P), nthreads)
+    rc = lib.oracle_attention_grouped(B, Tq, Tkv, h, h_kv, dk, dv, _ptr(Q), hdk, _ptr(K), h_kv * dk,
+                                      _ptr(V), kvw, int(bool(causal)), _iptr(kvl), _iptr(rws),
+                                      0 if rws is None else len(rws), _ptr(O), hdv, _ptr(P),
+                                      nthreads)
     if rc:
         raise ValueError(f"oracle_attention failed ({rc})")
     return (O, P) if return_weights else O
 
 
+def proj_width(h: int, d_k: int, d_v: int, h_kv=None, gated: bool = False) -> int:
+    """Columns of the fused projection: [Q | K | V (| G)]."""
+    h_kv = h if h_kv is None else int(h_kv)
+    return h * d_k + h_kv * d_k + h_kv * d_v + (h * d_v if gated else 0)
+
+
 def mha_forward(Xq, Wqkv, bqkv, Wo, bo, h: int, d_k: int, d_v: int, Xkv=None,
-                causal: bool = False, kv_lengths=None, rows=None, nthreads: int = 0):
+                causal: bool = False, kv_lengths=None, rows=None, nthreads: int = 0,
+                h_kv=None, gated: bool = False, residual=None):
     """The whole forward.  Xq (B,Tq,D); Xkv (B,Tkv,D) or None (self-attention);
-    Wqkv (D, 2*h*d_k + h*d_v) with column blocks [Q|K|V]; Wo (h*d_v, D).
-    rows: optional query-row indices (shared by every batch) to compute.
-    Returns Y (B, n_out, D) in fp64."""
+    Wqkv (D, proj_width(...)) with column blocks [Q|K|V(|G)]; Wo (h*d_v, D).
+    h_kv: K/V heads (default h); gated: sigmoid output gate from the G block;
+    residual: (B,Tq,D) added to Y.  rows: optional query-row indices (shared by every
+    batch) to compute.  Returns Y (B, n_out, D) in fp64."""
     lib = _load()
     Xq = _f64(Xq)
     Xkv = _f64(Xkv)
@@ -165,17 +198,47 @@ def mha_forward(Xq, Wqkv, bqkv, Wo, bo, h: int, d_k: int, d_v: int, Xkv=None,
     bqkv = _f64(bqkv)
     Wo = _f64(Wo)
     bo = _f64(bo)
+    R = _f64(residual)
+    h_kv = h if h_kv is None else int(h_kv)
     B, Tq, D = Xq.shape
     Tkv = Tq if Xkv is None else Xkv.shape[1]
-    if Wqkv.shape != (D, 2 * h * d_k + h * d_v) or Wo.shape != (h * d_v, D):
-        raise ValueError("weight shapes do not match (D, h, d_k, d_v)")
+    if Wqkv.shape != (D, proj_width(h, d_k, d_v, h_kv, gated)) or Wo.shape != (h * d_v, D):
+        raise ValueError("weight shapes do not match (D, h, h_kv, d_k, d_v, gated)")
+    if R is not None and R.shape != (B, Tq, D):
+        raise ValueError("residual must be (B, Tq, D)")
     kvl = _i32(kv_lengths)
     rws = _i32(rows)
     n_out = Tq if rws is None else len(rws)
     Y = np.empty((B, n_out, D), dtype=np.float64)
-    rc = lib.oracle_mha_forward(B, Tq, Tkv, D, h, d_k, d_v, _ptr(Xq), _ptr(Xkv), _ptr(Wqkv),
-                                _ptr(bqkv), _ptr(Wo), _ptr(bo), int(bool(causal)), _iptr(kvl),
-                                _iptr(rws), 0 if rws is None else len(rws), _ptr(Y), nthreads)
+    rc = lib.oracle_mha_forward_ex(B, Tq, Tkv, D, h, h_kv, d_k, d_v, int(bool(gated)), _ptr(Xq),
+                                   _ptr(Xkv), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), _ptr(R),
+                                   int(bool(causal)), _iptr(kvl), _iptr(rws),
+                                   0 if rws is None else len(rws), _ptr(Y), nthreads)
     if rc:
-        raise ValueError(f"oracle_mha_forward failed ({rc})")
+        raise ValueError(f"oracle_mha_forward_ex failed ({rc})")
     return Y
+
+
+def decode(Q, Kc, Vc, h: int, cache_lengths, h_kv=None, nthreads: int = 0):
+    """One decode step: new query rows Q (B,Tq,h*dk) over the cache Kc (B,Tmax,h_kv*dk),
+    Vc (B,Tmax,h_kv*dv); cache_lengths L_b count the cached tokens including the Tq new
+    ones (the last Tq of them).  Returns O (B, Tq, h*dv)."""
+    lib = _load()
+    Q = _f64(Q)
+    Kc = _f64(Kc)
+    Vc = _f64(Vc)
+    h_kv = h if h_kv is None else int(h_kv)
+    B, Tq, hdk = Q.shape
+    _, Tmax, kvw = Vc.shape
+    if hdk % h or kvw % h_kv or h % h_kv:
+        raise ValueError("head counts do not divide the widths")
+    dk, dv = hdk // h, kvw // h_kv
+    if Kc.shape != (B, Tmax, h_kv * dk):
+        raise ValueError("K cache width is not h_kv * d_k")
+    lens = _i32(cache_lengths)
+    O = np.empty((B, Tq, h * dv), dtype=np.float64)
+    rc = lib.oracle_decode(B, Tq, Tmax, h, h_kv, dk, dv, _ptr(Q), hdk, _ptr(Kc), h_kv * dk, _ptr(Vc),
+                           kvw, _iptr(lens), _ptr(O), h * dv, nthreads)
+    if rc:
+        raise ValueError(f"oracle_decode failed ({rc})")
+    return O

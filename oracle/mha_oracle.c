@@ -26,12 +26,32 @@
  *   molayo1419.me "MHA란 무엇인가?", pitfall 2/3: key padding excludes keys; a
  *     row whose keys are all excluded has an undefined softmax (NaN).
  *
+ * Variants (same pages):
+ *   - residual (iamjaehka13.blog, sections 14 and 16): X' = X + O W_O; here the
+ *     residual is any (B, T_q, D) tensor added to Y, normally X_q itself;
+ *   - grouped K/V heads, MQA / GQA (itwiki.kr "멀티 헤드 어텐션", section 추론 비용과
+ *     변형, its table): h query heads share h_kv K/V head sets, h_kv = 1 is MQA and
+ *     h_kv = h is plain MHA;
+ *   - gated attention (same section): a per-head sigmoid gate multiplies the scaled
+ *     dot-product attention output before W^O;
+ *   - KV-cache decode (same section): new query rows attend to the key/value cache
+ *     of the tokens so far.
+ *
  * Readings of points the pages leave open (each also listed in the design notes):
  *   - weights are (in, out) row-major so that Y = X W + b;
  *   - key padding is given as a per-batch valid length L_b: keys j >= L_b are
  *     masked; L_b outside [1, T_kv] is invalid and its rows come out NaN;
  *   - causal masking is defined only for T_q == T_kv (top-left aligned);
- *   - causal and padding masks combine by logical OR.
+ *   - causal and padding masks combine by logical OR;
+ *   - grouped heads: query head i uses K/V head i / (h / h_kv) (consecutive query heads
+ *     form a group); the fused projection's column blocks are [Q | K | V], of widths
+ *     h*d_k, h_kv*d_k, h_kv*d_v;
+ *   - the gate is elementwise and head-specific: G = sigmoid(X_q W_G + b_G), W_G of
+ *     shape (D, h*d_v) stored as a fourth column block of the fused projection, and
+ *     O_cat is multiplied by G element by element;
+ *   - decode: the T_q new tokens are the last T_q of each batch's L_b cached tokens,
+ *     so new token t sees cache entries j <= L_b - T_q + t (causal, bottom-aligned);
+ *     L_b < T_q or L_b > T_max is invalid and gives NaN rows.
  *
  * Precision: every operation is IEEE fp64; exp is libm exp().
  * Threads: OpenMP over independent output rows / (batch, head) pairs; the
@@ -116,14 +136,15 @@ int oracle_linear(long M, long K, long N,
  *   o_e = sum_j w_j v_je
  * The whole score row is materialised before the softmax.
  */
-int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
-                     const double* Q, long ldq,
-                     const double* K, long ldk,
-                     const double* V, long ldv,
-                     int causal, const int* kv_lengths,
-                     const int* rows, int n_rows,
-                     double* O, long ldo, double* P, int nthreads) {
+int oracle_attention_grouped(int B, int Tq, int Tkv, int h, int h_kv, int dk, int dv,
+                             const double* Q, long ldq,
+                             const double* K, long ldk,
+                             const double* V, long ldv,
+                             int causal, const int* kv_lengths,
+                             const int* rows, int n_rows,
+                             double* O, long ldo, double* P, int nthreads) {
     if (B < 0 || Tq < 0 || Tkv < 0 || h <= 0 || dk <= 0 || dv <= 0) return ORACLE_BAD_ARG;
+    if (h_kv <= 0 || h % h_kv != 0) return ORACLE_BAD_ARG;
     if (!Q || !K || !V || !O) return ORACLE_BAD_ARG;
     if (causal && Tq != Tkv) return ORACLE_BAD_ARG;
     const int n_out = rows ? n_rows : Tq;
@@ -138,6 +159,7 @@ int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
     for (bh = 0; bh < (long)B * h; ++bh) {
         const int b = (int)(bh / h);
         const int i = (int)(bh % h);
+        const int g = i / (h / h_kv); /* the K/V head of query head i */
         const int L = kv_lengths ? kv_lengths[b] : Tkv;
         const int valid_len = (L >= 1 && L <= Tkv);
         double* s = (double*)malloc(sizeof(double) * (size_t)(Tkv > 0 ? Tkv : 1));
@@ -161,7 +183,7 @@ int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
             }
             /* scores, scaled, masked */
             for (int j = 0; j < Tkv; ++j) {
-                const double* kj = K + ((long)b * Tkv + j) * ldk + (long)i * dk;
+                const double* kj = K + ((long)b * Tkv + j) * ldk + (long)g * dk;
                 double dot = 0.0;
                 for (int e = 0; e < dk; ++e) dot += q[e] * kj[e];
                 s[j] = dot * scale;
@@ -182,7 +204,7 @@ int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
             for (int e = 0; e < dv; ++e) o[e] = 0.0;
             for (int j = 0; j < Tkv; ++j) {
                 const double w = s[j];
-                const double* vj = V + ((long)b * Tkv + j) * ldv + (long)i * dv;
+                const double* vj = V + ((long)b * Tkv + j) * ldv + (long)g * dv;
                 for (int e = 0; e < dv; ++e) o[e] += w * vj[e];
             }
         }
@@ -191,30 +213,47 @@ int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
     return status;
 }
 
+/* Plain multi-head attention: every query head has its own K/V head. */
+int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
+                     const double* Q, long ldq,
+                     const double* K, long ldk,
+                     const double* V, long ldv,
+                     int causal, const int* kv_lengths,
+                     const int* rows, int n_rows,
+                     double* O, long ldo, double* P, int nthreads) {
+    return oracle_attention_grouped(B, Tq, Tkv, h, h, dk, dv, Q, ldq, K, ldk, V, ldv, causal,
+                                    kv_lengths, rows, n_rows, O, ldo, P, nthreads);
+}
+
 /*
- * The whole forward: projections, attention of every head, Concat, W^O.
+ * The whole forward: projections, attention of every head, Concat, W^O, and the
+ * variants (grouped K/V heads, output gate, residual).
  *
  *   Xq  (B, Tq, D);  Xkv (B, Tkv, D), or NULL for self-attention (Xkv = Xq)
- *   Wqkv (D, 2*h*dk + h*dv), column blocks [Q | K | V]; bqkv the same width or NULL
+ *   Wqkv (D, h*dk + h_kv*dk + h_kv*dv [+ h*dv if gated]), column blocks
+ *        [Q | K | V (| G)]; bqkv the same width or NULL
  *   Wo  (h*dv, D); bo (D) or NULL
+ *   R   (B, Tq, D) residual or NULL
  *   Y   (B, n_out, D) where n_out = n_rows if rows != NULL else Tq
  *
  * Only the query rows asked for are projected; every key/value row is
  * projected.  Steps:
- *   Qf = Xq  Wqkv[:, 0:h*dk]        + bqkv[0:h*dk]
- *   Kf = Xkv Wqkv[:, h*dk:2*h*dk]   + bqkv[h*dk:2*h*dk]
- *   Vf = Xkv Wqkv[:, 2*h*dk:]       + bqkv[2*h*dk:]
- *   Ocat = attention(Qf, Kf, Vf)     (head i at columns i*dv)
- *   Y  = Ocat Wo + bo
+ *   Qf = Xq  W[:, Q block] + b[Q block]
+ *   Kf = Xkv W[:, K block] + b[K block]
+ *   Vf = Xkv W[:, V block] + b[V block]
+ *   Ocat = attention(Qf, Kf, Vf)      (head i at columns i*dv, K/V head i/(h/h_kv))
+ *   if gated:  Gf = Xq W[:, G block] + b[G block];  Ocat *= 1 / (1 + exp(-Gf))
+ *   Y  = Ocat Wo + bo  (+ R)
  */
-int oracle_mha_forward(int B, int Tq, int Tkv, int D, int h, int dk, int dv,
-                       const double* Xq, const double* Xkv,
-                       const double* Wqkv, const double* bqkv,
-                       const double* Wo, const double* bo,
-                       int causal, const int* kv_lengths,
-                       const int* rows, int n_rows,
-                       double* Y, int nthreads) {
+int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk, int dv,
+                          int gated, const double* Xq, const double* Xkv,
+                          const double* Wqkv, const double* bqkv,
+                          const double* Wo, const double* bo, const double* R,
+                          int causal, const int* kv_lengths,
+                          const int* rows, int n_rows,
+                          double* Y, int nthreads) {
     if (B < 0 || Tq < 0 || Tkv < 0 || D <= 0 || h <= 0 || dk <= 0 || dv <= 0) return ORACLE_BAD_ARG;
+    if (h_kv <= 0 || h % h_kv != 0) return ORACLE_BAD_ARG;
     if (!Xq || !Wqkv || !Wo || !Y) return ORACLE_BAD_ARG;
     if (!Xkv) {
         Xkv = Xq;
@@ -222,15 +261,17 @@ int oracle_mha_forward(int B, int Tq, int Tkv, int D, int h, int dk, int dv,
     }
     if (causal && Tq != Tkv) return ORACLE_BAD_ARG;
     const int n_out = rows ? n_rows : Tq;
-    const long hq = (long)h * dk, hv = (long)h * dv;
-    const long wcols = 2 * hq + hv;
+    const long hq = (long)h * dk, hk = (long)h_kv * dk, hkv = (long)h_kv * dv, hv = (long)h * dv;
+    const long wcols = hq + hk + hkv + (gated ? hv : 0);
+    const long k_off = hq, v_off = hq + hk, g_off = hq + hk + hkv;
     double* Xsel = (double*)malloc(sizeof(double) * (size_t)((long)B * n_out * D + 1));
     double* Qf = (double*)malloc(sizeof(double) * (size_t)((long)B * n_out * hq + 1));
-    double* Kf = (double*)malloc(sizeof(double) * (size_t)((long)B * Tkv * hq + 1));
-    double* Vf = (double*)malloc(sizeof(double) * (size_t)((long)B * Tkv * hv + 1));
+    double* Kf = (double*)malloc(sizeof(double) * (size_t)((long)B * Tkv * hk + 1));
+    double* Vf = (double*)malloc(sizeof(double) * (size_t)((long)B * Tkv * hkv + 1));
     double* Oc = (double*)malloc(sizeof(double) * (size_t)((long)B * n_out * hv + 1));
+    double* Gf = gated ? (double*)malloc(sizeof(double) * (size_t)((long)B * n_out * hv + 1)) : NULL;
     int rc = ORACLE_OK;
-    if (!Xsel || !Qf || !Kf || !Vf || !Oc) {
+    if (!Xsel || !Qf || !Kf || !Vf || !Oc || (gated && !Gf)) {
         rc = ORACLE_NO_MEM;
         goto done;
     }
@@ -246,9 +287,11 @@ int oracle_mha_forward(int B, int Tq, int Tkv, int D, int h, int dk, int dv,
         }
     rc = oracle_linear((long)B * n_out, D, hq, Xsel, D, Wqkv, wcols, bqkv, Qf, hq, nthreads);
     if (rc) goto done;
-    rc = oracle_linear((long)B * Tkv, D, hq, Xkv, D, Wqkv + hq, wcols, bqkv ? bqkv + hq : NULL, Kf, hq, nthreads);
+    rc = oracle_linear((long)B * Tkv, D, hk, Xkv, D, Wqkv + k_off, wcols, bqkv ? bqkv + k_off : NULL, Kf,
+                       hk, nthreads);
     if (rc) goto done;
-    rc = oracle_linear((long)B * Tkv, D, hv, Xkv, D, Wqkv + 2 * hq, wcols, bqkv ? bqkv + 2 * hq : NULL, Vf, hv, nthreads);
+    rc = oracle_linear((long)B * Tkv, D, hkv, Xkv, D, Wqkv + v_off, wcols, bqkv ? bqkv + v_off : NULL, Vf,
+                       hkv, nthreads);
     if (rc) goto done;
     {
         /* the attention step sees the selected rows as a (B, n_out) query
@@ -264,21 +307,119 @@ int oracle_mha_forward(int B, int Tq, int Tkv, int D, int h, int dk, int dv,
                 for (int r = 0; r < n_out; ++r)
                     memcpy(Qfull + ((long)b * Tq + rows[r]) * hq, Qf + ((long)b * n_out + r) * hq,
                            sizeof(double) * (size_t)hq);
-            rc = oracle_attention(B, Tq, Tkv, h, dk, dv, Qfull, hq, Kf, hq, Vf, hv, causal, kv_lengths,
-                                  rows, n_rows, Oc, hv, NULL, nthreads);
+            rc = oracle_attention_grouped(B, Tq, Tkv, h, h_kv, dk, dv, Qfull, hq, Kf, hk, Vf, hkv, causal,
+                                          kv_lengths, rows, n_rows, Oc, hv, NULL, nthreads);
             free(Qfull);
         } else {
-            rc = oracle_attention(B, Tq, Tkv, h, dk, dv, Qf, hq, Kf, hq, Vf, hv, causal, kv_lengths, NULL, 0,
-                                  Oc, hv, NULL, nthreads);
+            rc = oracle_attention_grouped(B, Tq, Tkv, h, h_kv, dk, dv, Qf, hq, Kf, hk, Vf, hkv, causal,
+                                          kv_lengths, NULL, 0, Oc, hv, NULL, nthreads);
         }
         if (rc) goto done;
     }
+    if (gated) {
+        /* the gate of every output element, from the query-side input */
+        rc = oracle_linear((long)B * n_out, D, hv, Xsel, D, Wqkv + g_off, wcols, bqkv ? bqkv + g_off : NULL,
+                           Gf, hv, nthreads);
+        if (rc) goto done;
+        for (long e = 0; e < (long)B * n_out * hv; ++e) Oc[e] = Oc[e] * (1.0 / (1.0 + exp(-Gf[e])));
+    }
     rc = oracle_linear((long)B * n_out, hv, D, Oc, hv, Wo, D, bo, Y, D, nthreads);
+    if (rc) goto done;
+    if (R) {
+        for (int b = 0; b < B; ++b)
+            for (int r = 0; r < n_out; ++r) {
+                const int t = rows ? rows[r] : r;
+                const double* rr = R + ((long)b * Tq + t) * D;
+                double* y = Y + ((long)b * n_out + r) * D;
+                for (int c = 0; c < D; ++c) y[c] += rr[c];
+            }
+    }
 done:
     free(Xsel);
     free(Qf);
     free(Kf);
     free(Vf);
     free(Oc);
+    free(Gf);
     return rc;
+}
+
+/* The plain forward: h K/V heads, no gate, no residual. */
+int oracle_mha_forward(int B, int Tq, int Tkv, int D, int h, int dk, int dv,
+                       const double* Xq, const double* Xkv,
+                       const double* Wqkv, const double* bqkv,
+                       const double* Wo, const double* bo,
+                       int causal, const int* kv_lengths,
+                       const int* rows, int n_rows,
+                       double* Y, int nthreads) {
+    return oracle_mha_forward_ex(B, Tq, Tkv, D, h, h, dk, dv, 0, Xq, Xkv, Wqkv, bqkv, Wo, bo, NULL,
+                                 causal, kv_lengths, rows, n_rows, Y, nthreads);
+}
+
+/*
+ * Attention of new query rows over a key/value cache (one decode step).
+ *
+ * Q  (B, Tq) rows of stride ldq, head i at columns [i*dk, (i+1)*dk);
+ * Kc (B, Tmax) rows of stride ldk, K/V head g at columns [g*dk, (g+1)*dk);
+ * Vc (B, Tmax) rows of stride ldv, K/V head g at columns [g*dv, (g+1)*dv);
+ * cache_lengths: L_b per batch, the tokens cached so far including the Tq new ones;
+ * O  (B, Tq) rows of stride ldo, head i at columns [i*dv, (i+1)*dv).
+ *
+ * New row t of batch b is token L_b - Tq + t and sees cache entries
+ * j <= L_b - Tq + t; query head i uses K/V head i / (h / h_kv).  Per row:
+ *   s_j = (sum_e q_e k_je) / sqrt(dk)   for visible j
+ *   w_j = exp(s_j - max s) / sum exp(s - max s),   o_e = sum_j w_j v_je
+ */
+int oracle_decode(int B, int Tq, int Tmax, int h, int h_kv, int dk, int dv,
+                  const double* Q, long ldq, const double* Kc, long ldk, const double* Vc, long ldv,
+                  const int* cache_lengths, double* O, long ldo, int nthreads) {
+    if (B < 0 || Tq <= 0 || Tmax <= 0 || h <= 0 || dk <= 0 || dv <= 0) return ORACLE_BAD_ARG;
+    if (h_kv <= 0 || h % h_kv != 0 || !Q || !Kc || !Vc || !O || !cache_lengths) return ORACLE_BAD_ARG;
+    set_threads(nthreads);
+    const double scale = 1.0 / sqrt((double)dk);
+    int status = ORACLE_OK;
+    long bh;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (bh = 0; bh < (long)B * h; ++bh) {
+        const int b = (int)(bh / h);
+        const int i = (int)(bh % h);
+        const int g = i / (h / h_kv);
+        const int L = cache_lengths[b];
+        double* s = (double*)malloc(sizeof(double) * (size_t)Tmax);
+        if (!s) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEM;
+            continue;
+        }
+        for (int t = 0; t < Tq; ++t) {
+            double* o = O + ((long)b * Tq + t) * ldo + (long)i * dv;
+            if (L < Tq || L > Tmax) {
+                for (int e = 0; e < dv; ++e) o[e] = NAN;
+                continue;
+            }
+            const int n = L - Tq + t + 1; /* visible cache entries [0, n) */
+            const double* q = Q + ((long)b * Tq + t) * ldq + (long)i * dk;
+            double m = -INFINITY;
+            for (int j = 0; j < n; ++j) {
+                const double* kj = Kc + ((long)b * Tmax + j) * ldk + (long)g * dk;
+                double dot = 0.0;
+                for (int e = 0; e < dk; ++e) dot += q[e] * kj[e];
+                s[j] = dot * scale;
+                if (s[j] > m) m = s[j];
+            }
+            double sum = 0.0;
+            for (int j = 0; j < n; ++j) {
+                s[j] = exp(s[j] - m);
+                sum += s[j];
+            }
+            for (int e = 0; e < dv; ++e) o[e] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                const double w = s[j] / sum;
+                const double* vj = Vc + ((long)b * Tmax + j) * ldv + (long)g * dv;
+                for (int e = 0; e < dv; ++e) o[e] += w * vj[e];
+            }
+        }
+        free(s);
+    }
+    return status;
 }

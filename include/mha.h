@@ -73,6 +73,24 @@ typedef enum {
  */
 mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype);
 
+/*
+ * mha_create_ex -- mha_create with the variants of itwiki.kr "멀티 헤드 어텐션", section
+ * 추론 비용과 변형:
+ *   h_kv   number of K/V heads, a divisor of h: h_kv == h is plain multi-head attention,
+ *          h_kv == 1 multi-query attention (MQA), anything between grouped-query attention
+ *          (GQA).  Query head i uses K/V head i / (h / h_kv) (consecutive query heads form
+ *          a group).
+ *   gated  0 or 1: gated attention -- the output of every head is multiplied element by
+ *          element by sigmoid(X_q W_G + b_G) (a head-specific sigmoid gate on the scaled
+ *          dot-product attention output) before the output projection.
+ * The fused projection W_qkv then has the column blocks [W^Q | W^K | W^V (| W^G)] of widths
+ * h*d_k, h_kv*d_k, h_kv*d_v (and h*d_v).  MHA_ERR_INVALID_ARG as for mha_create, and for
+ * h_kv not dividing h or gated not 0/1.  mha_create(D, h, d_k, d_v) is
+ * mha_create_ex(D, h, h, d_k, d_v, 0).
+ */
+mha_status mha_create_ex(mha_t* out, int D, int h, int h_kv, int d_k, int d_v, int gated,
+                         mha_dtype dtype);
+
 /* mha_destroy -- free the handle (NULL is ignored).  Does not touch the
  * caller's workspace. */
 void mha_destroy(mha_t handle);
@@ -80,10 +98,10 @@ void mha_destroy(mha_t handle);
 /*
  * mha_workspace_size -- bytes of device workspace mha_forward needs for
  * batch B, T_q query rows and T_kv key rows (self-attention: T_kv = T_q).
- * Layout: a 256-byte status block, the projected Q (B,T_q,h*d_k) and K,V
- * (B,T_kv,h*(d_k+d_v)) -- for self-attention one (B,T,2h*d_k+h*d_v) buffer
- * -- and Ocat (B,T_q,h*d_v), each 256-byte aligned.  Returns 0 for an invalid
- * handle or size.
+ * Layout: a 256-byte status block, the projected query side Q (and the gate
+ * pre-activations) (B,T_q,h*d_k [+h*d_v]) and K,V (B,T_kv,h_kv*(d_k+d_v)) -- for
+ * self-attention one fused buffer of the projection's width -- and Ocat
+ * (B,T_q,h*d_v), each 256-byte aligned.  Returns 0 for an invalid handle or size.
  */
 size_t mha_workspace_size(mha_t handle, int B, int T_q, int T_kv);
 
@@ -123,6 +141,22 @@ mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, i
                        int causal, const int32_t* kv_lengths, void* out, void* stream);
 
 /*
+ * mha_forward_ex -- mha_forward for a handle of any mha_create_ex shape (W_qkv with the
+ * column blocks described there), plus an optional residual:
+ *   residual  (B, T_q, D) or NULL; added to the output in the output projection's epilogue,
+ *             Y = residual + Concat(heads) W_o + b_o (iamjaehka13.blog "[Deep Learning 5]
+ *             Attention의 내부 계산", sections 14 and 16: X' = X + O W_O, so normally
+ *             residual == X_q).  It may be `out` itself (in place) but must not otherwise
+ *             overlap it (MHA_ERR_INVALID_ARG); bf16 needs it 16-byte aligned.
+ * With a gate and X_kv != X_q the gate pre-activations come from X_q (one more GEMM).
+ * mha_forward(...) is mha_forward_ex(..., residual = NULL, out, stream).
+ */
+mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q,
+                          int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                          const void* b_o, int causal, const int32_t* kv_lengths,
+                          const void* residual, void* out, void* stream);
+
+/*
  * mha_linear -- one projection step, C = A W + bias
  * (itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영).
  *   A (M, K) row stride lda;  W (K, N) row stride ldw;  bias (N) or NULL;
@@ -150,6 +184,48 @@ mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv,
                          const void* Q, int64_t ldq, const void* K, int64_t ldk,
                          const void* V, int64_t ldv, int causal, const int32_t* kv_lengths,
                          void* O, int64_t ldo, void* stream);
+
+/*
+ * mha_attention_ex -- mha_attention with the handle's K/V head count and an optional gate.
+ *   K, V  head g of the h_kv K/V heads at columns [g*d_k, (g+1)*d_k) / [g*d_v, (g+1)*d_v);
+ *         query head i reads K/V head i / (h / h_kv)
+ *   G     NULL, or the gate pre-activations, rows (B, T_q) of stride ldg, head i at
+ *         columns [i*d_v, (i+1)*d_v): O = softmax(...) V * sigmoid(G), element by element
+ * mha_attention(...) is mha_attention_ex(..., G = NULL, ldg = 0, ...).
+ */
+mha_status mha_attention_ex(mha_t handle, int B, int T_q, int T_kv,
+                            const void* Q, int64_t ldq, const void* K, int64_t ldk,
+                            const void* V, int64_t ldv, const void* G, int64_t ldg, int causal,
+                            const int32_t* kv_lengths, void* O, int64_t ldo, void* stream);
+
+/*
+ * mha_decode_workspace_size -- bytes of workspace mha_decode needs: the 256-byte status
+ * block and, for bf16, the per-chunk partial results of the split over the cache (B*h*T_q
+ * rows, one (max, sum, d_v values) record per 128 cached tokens).  0 for an invalid handle.
+ */
+size_t mha_decode_workspace_size(mha_t handle, int B, int T_q, int T_max);
+
+/*
+ * mha_decode -- one decode step over a key/value cache (itwiki.kr "멀티 헤드 어텐션",
+ * section 추론 비용과 변형: generation keeps the keys and values of earlier tokens and
+ * every step reads the whole cache, so the step is bound by memory bandwidth).
+ *   Q        the T_q new tokens' queries, rows (B, T_q) of stride ldq, head i at columns
+ *            [i*d_k, (i+1)*d_k)
+ *   K_cache  rows (B, T_max) of stride ldk, K/V head g at columns [g*d_k, (g+1)*d_k)
+ *   V_cache  rows (B, T_max) of stride ldv, K/V head g at columns [g*d_v, (g+1)*d_v)
+ *   cache_lengths  device int32[B]: L_b cached tokens, the T_q new ones included (their keys
+ *            and values already written at rows L_b - T_q .. L_b - 1)
+ *   O        rows (B, T_q) of stride ldo, head i at columns [i*d_v, (i+1)*d_v)
+ * New token t sees cache rows j <= L_b - T_q + t; query head i uses K/V head i / (h / h_kv).
+ * L_b outside [T_q, T_max] makes that batch's rows NaN and records MHA_ERR_BAD_LENGTH.
+ * bf16 (d_k == d_v in {64, 128}) splits the cache over many CTAs and needs a workspace of
+ * mha_decode_workspace_size bytes (MHA_ERR_WORKSPACE otherwise); fp32 (d_k, d_v <= 256) needs
+ * none.  B == 0 or T_q == 0 is a no-op; T_q > T_max or cache_lengths == NULL is
+ * MHA_ERR_INVALID_ARG.  Launches two kernels (bf16) or one (fp32) on `stream`.
+ */
+mha_status mha_decode(mha_t handle, int B, int T_q, int T_max, const void* Q, int64_t ldq,
+                      const void* K_cache, int64_t ldk, const void* V_cache, int64_t ldv,
+                      const int32_t* cache_lengths, void* O, int64_t ldo, void* stream);
 
 /*
  * mha_get_status -- copy the device status word of the attached workspace to

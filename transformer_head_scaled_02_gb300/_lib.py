@@ -32,13 +32,19 @@ _sz = ctypes.c_size_t
 
 _SIGNATURES = {
     "mha_create": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i]),
+    "mha_create_ex": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i]),
     "mha_destroy": (None, [_vp]),
     "mha_workspace_size": (_sz, [_vp, _i, _i, _i]),
     "mha_set_workspace": (_i, [_vp, _vp, _sz]),
     "mha_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp]),
+    "mha_forward_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
     "mha_linear": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp]),
     "mha_attention": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i64,
                            _vp]),
+    "mha_attention_ex": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp,
+                              _vp, _i64, _vp]),
+    "mha_decode_workspace_size": (_sz, [_vp, _i, _i, _i]),
+    "mha_decode": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp]),
     "mha_get_status": (_i, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "mha_forward_static_workspace": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp,
                                           _vp, _vp]),
@@ -95,6 +101,13 @@ def mha_create(D: int, h: int, d_k: int, d_v: int, dtype: int) -> int:
     return out.value
 
 
+def mha_create_ex(D: int, h: int, h_kv: int, d_k: int, d_v: int, gated: int, dtype: int) -> int:
+    out = _vp()
+    _check("mha_create_ex", load().mha_create_ex(ctypes.byref(out), D, h, h_kv, d_k, d_v, int(gated),
+                                                 dtype))
+    return out.value
+
+
 def mha_destroy(handle: int) -> None:
     load().mha_destroy(handle)
 
@@ -114,6 +127,13 @@ def mha_forward(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal,
     return _check("mha_forward", code) if check else code
 
 
+def mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal, kv_lengths,
+                   residual, out, stream, check: bool = True) -> int:
+    code = load().mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o,
+                                 int(causal), kv_lengths, residual, out, stream)
+    return _check("mha_forward_ex", code) if check else code
+
+
 def mha_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc, stream, check: bool = True) -> int:
     code = load().mha_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc, stream)
     return _check("mha_linear", code) if check else code
@@ -124,6 +144,24 @@ def mha_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengt
     code = load().mha_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, int(causal),
                                 kv_lengths, O, ldo, stream)
     return _check("mha_attention", code) if check else code
+
+
+def mha_attention_ex(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, G, ldg, causal, kv_lengths, O,
+                     ldo, stream, check: bool = True) -> int:
+    code = load().mha_attention_ex(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, G, ldg, int(causal),
+                                   kv_lengths, O, ldo, stream)
+    return _check("mha_attention_ex", code) if check else code
+
+
+def mha_decode_workspace_size(handle: int, B: int, T_q: int, T_max: int) -> int:
+    return int(load().mha_decode_workspace_size(handle, B, T_q, T_max))
+
+
+def mha_decode(handle, B, T_q, T_max, Q, ldq, K_cache, ldk, V_cache, ldv, cache_lengths, O, ldo,
+               stream, check: bool = True) -> int:
+    code = load().mha_decode(handle, B, T_q, T_max, Q, ldq, K_cache, ldk, V_cache, ldv,
+                             cache_lengths, O, ldo, stream)
+    return _check("mha_decode", code) if check else code
 
 
 def mha_get_status(handle: int, stream: int) -> int:

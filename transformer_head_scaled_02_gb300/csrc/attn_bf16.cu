@@ -184,13 +184,30 @@ __device__ __forceinline__ float exp_tile(const float (&x)[128], uint64_t c2, fl
     return a0 + a1;
 }
 
-template <int HD>
+// The output gate of gated attention: f[i] *= sigmoid(g_i) for 8 consecutive outputs, g the
+// gate pre-activations (bf16) of this row.  sigmoid(x) = 1 / (1 + 2^(-x log2 e)).
+__device__ __forceinline__ void apply_gate8(const __nv_bfloat16* g, float (&f)[8]) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(g));
+    const uint32_t gw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xFFFF0000u);
+        f[2 * i] *= __frcp_rn(1.f + ex2_approx(-1.4426950408889634f * g0));
+        f[2 * i + 1] *= __frcp_rn(1.f + ex2_approx(-1.4426950408889634f * g1));
+    }
+}
+
+// GATE: the epilogue multiplies by the sigmoid gate (a separate instantiation, so that plain
+// attention carries none of its code or registers).
+template <int HD, bool GATE>
 __global__ void __launch_bounds__(A_THREADS, 1)
     attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
-                        const __grid_constant__ CUtensorMap tmO, int h, int T_q, int T_kv, int causal,
-                        const int32_t* __restrict__ kv_lengths, float scale_log2, int* status) {
+                        const __grid_constant__ CUtensorMap tmO, int h, int h_kv, int T_q, int T_kv,
+                        int causal, const int32_t* __restrict__ kv_lengths,
+                        const __nv_bfloat16* __restrict__ gate, int64_t ldg, float scale_log2,
+                        int* status) {
     using C = AttnCfg<HD>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -221,6 +238,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int bh = blockIdx.x;
     const int b = bh / h;
     const int head = bh - b * h;
+    const int kvh = head / (h / h_kv);  // grouped K/V heads: the K/V head of this query head
     const int qb = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
     const int q0 = qb * (C::NQ * C::BM);
 
@@ -290,12 +308,12 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::CH; ++c)
-                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tmK, head * HD + c * 64,
+                    tma_load_3d(sK + st * C::KV_BYTES + c * C::CHUNK, &tmK, kvh * HD + c * 64,
                                 j * C::BN, b, kb);
                 mbar_arrive_expect_tx(vb, C::KV_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::CH; ++c)
-                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tmV, head * HD + c * 64,
+                    tma_load_3d(sV + st * C::KV_BYTES + c * C::CHUNK, &tmV, kvh * HD + c * 64,
                                 j * C::BN, b, vb);
                 ++issued;
             }
@@ -553,7 +571,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                                                         abort_flag, status))) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                // O / l as bf16 into this tile's Q buffer (idle now), in the TMA box layout
+                const __nv_bfloat16* grow =
+                    GATE && row < T_q ? gate + ((int64_t)b * T_q + row) * ldg + (int64_t)head * HD : nullptr;
+                // O / l (times the gate) as bf16 into this tile's Q buffer (idle now), in the
+                // TMA box layout
 #pragma unroll
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t o[32];
@@ -566,6 +587,8 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
+                        if constexpr (GATE)
+                            if (grow != nullptr) apply_gate8(grow + cc * 32 + u4 * 8, f);
                         st_shared_v4(sQt + c * C::CHUNK + r * 128 + ((u ^ sw) << 4),
                                      pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
@@ -634,12 +657,12 @@ constexpr uint32_t D64_TMEM_COLS = 256;
 constexpr uint32_t D64_S_COL = 0, D64_O_COL = 128, D64_P_COL = 192;
 
 struct D64Item {
-    int b, head, qrow0, n;  // n = key tiles to visit (0: no valid key)
+    int b, head, kvh, qrow0, n;  // kvh: the K/V head; n = key tiles to visit (0: no valid key)
     bool bad;
 };
 
 // Item k of the longest-first numbering.
-__device__ __forceinline__ D64Item d64_item(int k, int BH, int h, int n_qt, int causal,
+__device__ __forceinline__ D64Item d64_item(int k, int BH, int h, int group, int n_qt, int causal,
                                             const int32_t* kv_lengths, int T_kv) {
     D64Item it;
     const int rank = k / BH;
@@ -647,6 +670,7 @@ __device__ __forceinline__ D64Item d64_item(int k, int BH, int h, int n_qt, int 
     const int qt = causal ? n_qt - 1 - rank : rank;
     it.b = bh / h;
     it.head = bh - it.b * h;
+    it.kvh = it.head / group;
     it.qrow0 = qt * 128;
     const int L = kv_lengths != nullptr ? kv_lengths[it.b] : T_kv;
     it.bad = L < 1 || L > T_kv;
@@ -661,12 +685,14 @@ __device__ __forceinline__ int d64_item_index(int r, int G, int c) {
     return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
+template <bool GATE>
 __global__ void __launch_bounds__(D64_THREADS, 2)
     attn_bf16_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmO, int B, int h, int T_q, int T_kv,
-                         int causal, const int32_t* __restrict__ kv_lengths, float scale_log2,
+                         const __grid_constant__ CUtensorMap tmO, int B, int h, int h_kv, int T_q,
+                         int T_kv, int causal, const int32_t* __restrict__ kv_lengths,
+                         const __nv_bfloat16* __restrict__ gate, int64_t ldg, float scale_log2,
                          int* status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -704,7 +730,7 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
     int R = 0;  // items of this CTA
     while (d64_item_index(R, G, c) < N) ++R;
     auto item = [&](int r) {
-        return d64_item(d64_item_index(r, G, c), BH, h, n_qt, causal, kv_lengths, T_kv);
+        return d64_item(d64_item_index(r, G, c), BH, h, h / h_kv, n_qt, causal, kv_lengths, T_kv);
     };
 
     if (threadIdx.x == 0) {
@@ -766,7 +792,7 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                     ok = mbar_wait(bar_kempty + 8u * st, ((gk / DK_STAGES) & 1u) ^ 1u, abort_flag, status);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar_kfull + 8u * st, D64_TILE);
-                    tma_load_3d(sK + st * D64_TILE, &tmK, it.head * 64, j * 128, it.b, bar_kfull + 8u * st);
+                    tma_load_3d(sK + st * D64_TILE, &tmK, it.kvh * 64, j * 128, it.b, bar_kfull + 8u * st);
                     ++gk;
                 }
             }
@@ -789,7 +815,7 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                     ok = mbar_wait(bar_vempty + 8u * st, ((gv / DV_STAGES) & 1u) ^ 1u, abort_flag, status);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar_vfull + 8u * st, D64_TILE);
-                    tma_load_3d(sV + st * D64_TILE, &tmV, it.head * 64, j * 128, it.b, bar_vfull + 8u * st);
+                    tma_load_3d(sV + st * D64_TILE, &tmV, it.kvh * 64, j * 128, it.b, bar_vfull + 8u * st);
                     ++gv;
                 }
             }
@@ -972,7 +998,10 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                 }
                 tc_fence_after();
                 const float inv = 1.f / l;
-                // O / l as bf16 into the item's Q buffer (its last score MMA has completed)
+                const __nv_bfloat16* grow =
+                    GATE && row < T_q ? gate + ((int64_t)it.b * T_q + row) * ldg + (int64_t)it.head * 64 : nullptr;
+                // O / l (times the gate) as bf16 into the item's Q buffer (its last score MMA
+                // has completed)
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t o[32];
@@ -984,6 +1013,8 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
+                        if constexpr (GATE)
+                            if (grow != nullptr) apply_gate8(grow + cc * 32 + u4 * 8, f);
                         st_shared_v4(sOut + r_ * 128 + (((uint32_t)u ^ sw) << 4),
                                      pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
@@ -1006,9 +1037,10 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
 }
 
 cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t ldk,
-                            const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
-                            int T_q, int T_kv, int causal, const int32_t* kv_lengths, int num_sms,
-                            int* status, cudaStream_t stream) {
+                            const void* V, int64_t ldv, const void* G, int64_t ldg, void* O,
+                            int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int causal,
+                            const int32_t* kv_lengths, int num_sms, int* status,
+                            cudaStream_t stream) {
     CUtensorMap tQ, tK, tV, tO;
     const uint32_t box[3] = {64, 128, 1};
     {
@@ -1017,12 +1049,12 @@ cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t l
         if (!encode_tmap_bf16(&tQ, Q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t dims[3] = {(uint64_t)h_kv * 64, (uint64_t)T_kv, (uint64_t)B};
         const uint64_t strides[2] = {(uint64_t)ldk * 2, (uint64_t)ldk * 2 * (uint64_t)T_kv};
         if (!encode_tmap_bf16(&tK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[3] = {(uint64_t)h * 64, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t dims[3] = {(uint64_t)h_kv * 64, (uint64_t)T_kv, (uint64_t)B};
         const uint64_t strides[2] = {(uint64_t)ldv * 2, (uint64_t)ldv * 2 * (uint64_t)T_kv};
         if (!encode_tmap_bf16(&tV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
@@ -1033,31 +1065,34 @@ cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t l
     }
     // setmaxnreg.inc waits until the CTA's register pool (threads x registers at launch) can
     // grant the rise: refuse to launch a build whose register count cannot cover the split
-    static int pool_ok = -1;
-    if (pool_ok < 0) {
+    static int pool_ok[2] = {-1, -1};
+    int& ok = pool_ok[G != nullptr];
+    if (ok < 0) {
         cudaFuncAttributes fa;
-        const cudaError_t e = cudaFuncGetAttributes(&fa, attn_bf16_d64_kernel);
+        const cudaError_t e = cudaFuncGetAttributes(
+            &fa, G != nullptr ? attn_bf16_d64_kernel<true> : attn_bf16_d64_kernel<false>);
         if (e != cudaSuccess) return e;
-        pool_ok = fa.numRegs * D64_THREADS >= 128 * (D64_REGS_CTRL + D64_REGS_SOFTMAX) ? 1 : 0;
+        ok = fa.numRegs * D64_THREADS >= 128 * (D64_REGS_CTRL + D64_REGS_SOFTMAX) ? 1 : 0;
     }
-    if (!pool_ok) return cudaErrorInvalidConfiguration;
-    cudaError_t err = cudaFuncSetAttribute(attn_bf16_d64_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, D64_SMEM);
+    if (!ok) return cudaErrorInvalidConfiguration;
+    auto kernel = G != nullptr ? attn_bf16_d64_kernel<true> : attn_bf16_d64_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D64_SMEM);
     if (err != cudaSuccess) return err;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt(64.0));
     const int64_t items = (int64_t)B * h * ((T_q + 127) / 128);
     if (items > INT32_MAX) return cudaErrorInvalidValue;
     const int64_t slots = 2 * (int64_t)(num_sms > 0 ? num_sms : 1);
     const int grid = (int)(items < slots ? items : slots);
-    return launch_pdl(attn_bf16_d64_kernel, dim3(grid), dim3(D64_THREADS), D64_SMEM, stream, tQ, tK, tV,
-                      tO, B, h, T_q, T_kv, causal, kv_lengths, scale_log2, status);
+    return launch_pdl(kernel, dim3(grid), dim3(D64_THREADS), D64_SMEM, stream, tQ, tK, tV,
+                      tO, B, h, h_kv, T_q, T_kv, causal, kv_lengths,
+                      reinterpret_cast<const __nv_bfloat16*>(G), ldg, scale_log2, status);
 }
 
 template <int HD>
 cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ldk, const void* V,
-                           int64_t ldv, void* O, int64_t ldo, int B, int h, int T_q, int T_kv,
-                           int causal, const int32_t* kv_lengths, int* status,
-                           cudaStream_t stream) {
+                           int64_t ldv, const void* G, int64_t ldg, void* O, int64_t ldo, int B,
+                           int h, int h_kv, int T_q, int T_kv, int causal,
+                           const int32_t* kv_lengths, int* status, cudaStream_t stream) {
     using C = AttnCfg<HD>;
     CUtensorMap tQ, tK, tV, tO;
     const uint32_t box[3] = {64, 128, 1};
@@ -1067,12 +1102,12 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
         if (!encode_tmap_bf16(&tQ, Q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[3] = {(uint64_t)h * HD, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t dims[3] = {(uint64_t)h_kv * HD, (uint64_t)T_kv, (uint64_t)B};
         const uint64_t strides[2] = {(uint64_t)ldk * 2, (uint64_t)ldk * 2 * (uint64_t)T_kv};
         if (!encode_tmap_bf16(&tK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[3] = {(uint64_t)h * HD, (uint64_t)T_kv, (uint64_t)B};
+        const uint64_t dims[3] = {(uint64_t)h_kv * HD, (uint64_t)T_kv, (uint64_t)B};
         const uint64_t strides[2] = {(uint64_t)ldv * 2, (uint64_t)ldv * 2 * (uint64_t)T_kv};
         if (!encode_tmap_bf16(&tV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
@@ -1081,22 +1116,24 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
         const uint64_t strides[2] = {(uint64_t)ldo * 2, (uint64_t)ldo * 2 * (uint64_t)T_q};
         if (!encode_tmap_bf16(&tO, O, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t err = cudaFuncSetAttribute(attn_bf16_tc_kernel<HD>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    auto kernel = G != nullptr ? attn_bf16_tc_kernel<HD, true> : attn_bf16_tc_kernel<HD, false>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (err != cudaSuccess) return err;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     const int rows_per_cta = C::NQ * C::BM;
     const dim3 grid((unsigned)(B * h), (unsigned)((T_q + rows_per_cta - 1) / rows_per_cta));
-    return launch_pdl(attn_bf16_tc_kernel<HD>, grid, dim3(A_THREADS), C::SMEM, stream, tQ, tK, tV, tO,
-                      h, T_q, T_kv, causal, kv_lengths, scale_log2, status);
+    return launch_pdl(kernel, grid, dim3(A_THREADS), C::SMEM, stream, tQ, tK, tV, tO,
+                      h, h_kv, T_q, T_kv, causal, kv_lengths, reinterpret_cast<const __nv_bfloat16*>(G),
+                      ldg, scale_log2, status);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t ldk,
-                             const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
-                             int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
-                             int num_sms, int* status, cudaStream_t stream) {
+                             const void* V, int64_t ldv, const void* G, int64_t ldg, void* O,
+                             int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d, int causal,
+                             const int32_t* kv_lengths, int num_sms, int* status,
+                             cudaStream_t stream) {
     // d = 64: causal self-attention without key lengths (query tiles of a head differ only in
     // their causal length, and the lengths are known here) runs on the persistent kernel,
     // whose fixed item order balances them; with key lengths (known only on the device) or
@@ -1104,13 +1141,13 @@ cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t 
     // two query tiles share each K/V tile and whose CTAs the hardware schedules as they
     // finish, is the better fit
     if (d == 64 && causal && kv_lengths == nullptr)
-        return launch_attn_d64(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
+        return launch_attn_d64(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
                                kv_lengths, num_sms, status, stream);
     if (d == 64)
-        return launch_attn_hd<64>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
+        return launch_attn_hd<64>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
                                   kv_lengths, status, stream);
     if (d == 128)
-        return launch_attn_hd<128>(Q, ldq, K, ldk, V, ldv, O, ldo, B, h, T_q, T_kv, causal,
+        return launch_attn_hd<128>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
                                    kv_lengths, status, stream);
     return cudaErrorInvalidValue;
 }

@@ -1,7 +1,9 @@
 // gemm_bf16.cu -- the projection steps on tcgen05 tensor cores:
-//   C = A W + bias    (A (M,K) bf16, W (K,N) bf16 (in,out) row-major, fp32 accumulate, C bf16)
+//   C = A W + bias (+ R)   (A (M,K) bf16, W (K,N) bf16 (in,out) row-major, fp32 accumulate,
+//                           optional bf16 residual R (M,N), C bf16)
 // which is [Q|K|V] = X W_qkv + b_qkv and Y = Ocat W_o + b_o of
-// itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영.
+// itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영, and the residual
+// form X' = X + O W_O of iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", section 14.
 //
 // Design (persistent, warp-specialised, one CTA per SM):
 //   warp 0      TMA producer: A tile 128x64 (K-major, 128B swizzle) and W tile 64x256
@@ -46,12 +48,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// RESID: the epilogue adds the residual R (a separate instantiation, so that the plain
+// projection carries none of its code or registers).
+template <bool RESID>
 __global__ void __launch_bounds__(G_THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmC,
-                        const __nv_bfloat16* __restrict__ bias, int M, int N, int K,
-                        int* status) {
+                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* R,
+                        int64_t ldr, int M, int N, int K, int* status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -220,11 +225,29 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
                 __syncwarp();
                 const uint32_t row = buf + (uint32_t)lane * 128u;
+                // this thread's 64 residual values (one 128-byte row segment), loaded up front
+                uint4 rres[RESID ? 8 : 1];
+                if constexpr (RESID) {
+                    const int grow = m0 + q * 32 + lane;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        rres[u] = grow < M && nc + u * 8 < N
+                                      ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)grow * ldr + nc + u * 8))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
+                    if constexpr (RESID) {
+                        const uint32_t rw[4] = {rres[u].x, rres[u].y, rres[u].z, rres[u].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            x[2 * i] += __uint_as_float(rw[i] << 16);
+                            x[2 * i + 1] += __uint_as_float(rw[i] & 0xFFFF0000u);
+                        }
+                    }
                     if (bias != nullptr && nc + u * 8 < N) {
                         const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
                         const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
@@ -283,12 +306,13 @@ constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + 10
 
 static_assert(P_SMEM <= 232448, "shared memory budget (pair)");
 
+template <bool RESID>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmC,
-                          const __nv_bfloat16* __restrict__ bias, int M, int N, int K,
-                          int* status) {
+                          const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* R,
+                          int64_t ldr, int M, int N, int K, int* status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -469,11 +493,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
                 const uint32_t row = buf + (uint32_t)lane * 128u;
+                // this thread's 64 residual values (one 128-byte row segment), loaded up front
+                uint4 rres[RESID ? 8 : 1];
+                if constexpr (RESID) {
+                    const int grow = m0 + q * 32 + lane;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        rres[u] = grow < M && nc + u * 8 < N
+                                      ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)grow * ldr + nc + u * 8))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
+                    if constexpr (RESID) {
+                        const uint32_t rw[4] = {rres[u].x, rres[u].y, rres[u].z, rres[u].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            x[2 * i] += __uint_as_float(rw[i] << 16);
+                            x[2 * i + 1] += __uint_as_float(rw[i] & 0xFFFF0000u);
+                        }
+                    }
                     if (bias != nullptr && nc + u * 8 < N) {
                         const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
                         const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
@@ -511,8 +553,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
-                             const void* bias, void* C, int64_t ldc, int M, int N, int K,
-                             int num_sms, int* status, cudaStream_t stream) {
+                             const void* bias, const void* R, int64_t ldr, void* C, int64_t ldc,
+                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream) {
     CUtensorMap tA, tW, tC;
     {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
@@ -533,16 +575,18 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         if (!encode_tmap_bf16(&tC, C, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
+    auto pair_kernel = R != nullptr ? gemm_bf16_pair_kernel<true> : gemm_bf16_pair_kernel<false>;
+    auto tc_kernel = R != nullptr ? gemm_bf16_tc_kernel<true> : gemm_bf16_tc_kernel<false>;
     if (M > 128) {
         // CTA pairs: the W box is 64 columns x 64 K-rows, the A box 64 K x 128 rows (as
         // above); each CTA of a pair loads its own A rows and its half of the W tile.
-        cudaError_t err = cudaFuncSetAttribute(gemm_bf16_pair_kernel,
+        cudaError_t err = cudaFuncSetAttribute(pair_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
         if (err != cudaSuccess) return err;
-        static int max_pairs_cache[64] = {0};
+        static int max_pairs_cache[2][64] = {{0}};
         int dev = 0;
         cudaGetDevice(&dev);
-        int max_pairs = dev >= 0 && dev < 64 ? max_pairs_cache[dev] : 0;
+        int max_pairs = dev >= 0 && dev < 64 ? max_pairs_cache[R != nullptr][dev] : 0;
         if (max_pairs == 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
@@ -556,22 +600,24 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+            if (cudaOccupancyMaxActiveClusters(&n, pair_kernel, &cfg) != cudaSuccess || n <= 0)
                 n = num_sms / 2;
             max_pairs = n;
-            if (dev >= 0 && dev < 64) max_pairs_cache[dev] = n;
+            if (dev >= 0 && dev < 64) max_pairs_cache[R != nullptr][dev] = n;
         }
         const int pair_tiles = ((M + 255) / 256) * ((N + G_BN - 1) / G_BN);
         const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-        return launch_pdl(gemm_bf16_pair_kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream,
-                          tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
+        return launch_pdl(pair_kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream,
+                          tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias),
+                          reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status);
     }
-    cudaError_t err = cudaFuncSetAttribute(gemm_bf16_tc_kernel,
+    cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (err != cudaSuccess) return err;
     const int grid = num_tiles < num_sms ? num_tiles : num_sms;
-    return launch_pdl(gemm_bf16_tc_kernel, dim3(grid), dim3(G_THREADS), G_SMEM, stream, tA, tW, tC,
-                      reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
+    return launch_pdl(tc_kernel, dim3(grid), dim3(G_THREADS), G_SMEM, stream, tA, tW, tC,
+                      reinterpret_cast<const __nv_bfloat16*>(bias),
+                      reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status);
 }
 
 }  // namespace mha

@@ -10,8 +10,10 @@
 #include "../../include/mha.h"
 
 // The opaque handle of include/mha.h: the layer configuration and the caller's workspace.
+// h_kv: K/V heads (h for plain multi-head attention, 1 for MQA); gated: the fused projection
+// carries a fourth block of h*d_v gate pre-activations.
 struct mha_s {
-    int D, h, dk, dv;
+    int D, h, h_kv, dk, dv, gated;
     mha_dtype dtype;
     void* ws;
     size_t ws_bytes;
@@ -46,28 +48,42 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
 
-// C = A W + bias, fp32 everywhere.  A (M,K) lda; W (K,N) ldw; C (M,N) ldc.
+// C = A W + bias (+ R), fp32 everywhere.  A (M,K) lda; W (K,N) ldw; R (M,N) ldr or null;
+// C (M,N) ldc.
 cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t ldw,
-                            const float* bias, float* C, int64_t ldc, int M, int N, int K,
+                            const float* bias, const float* R, int64_t ldr, float* C, int64_t ldc,
+                            int M, int N, int K, cudaStream_t stream);
+
+// Attention for all heads, fp32.  See mha_attention_ex in include/mha.h for the layout;
+// decode != 0 places the T_q rows at the end of each batch's L_b keys (mha_decode).
+cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,
+                            const float* V, int64_t ldv, const float* G, int64_t ldg, float* O,
+                            int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d_k, int d_v,
+                            int causal, int decode, const int32_t* kv_lengths, int* status,
                             cudaStream_t stream);
 
-// Attention for all heads, fp32.  See mha_attention in include/mha.h for the layout.
-cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,
-                            const float* V, int64_t ldv, float* O, int64_t ldo, int B, int h,
-                            int T_q, int T_kv, int d_k, int d_v, int causal,
-                            const int32_t* kv_lengths, int* status, cudaStream_t stream);
-
-// C = A W + bias on tcgen05: bf16 operands, fp32 accumulation in TMEM, bf16 output.
-// Requires K, N, lda, ldw, ldc multiples of 8 and 16-byte aligned pointers.
+// C = A W + bias (+ R) on tcgen05: bf16 operands, fp32 accumulation in TMEM, bf16 output.
+// Requires K, N, lda, ldw, ldc (and ldr) multiples of 8 and 16-byte aligned pointers.
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
-                             const void* bias, void* C, int64_t ldc, int M, int N, int K,
-                             int num_sms, int* status, cudaStream_t stream);
+                             const void* bias, const void* R, int64_t ldr, void* C, int64_t ldc,
+                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream);
 
-// Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v).  num_sms sizes the
-// persistent grid of the d = 64 kernel.
+// Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v), grouped K/V heads
+// (h_kv divides h) and an optional gate G.  num_sms sizes the persistent grid of the d = 64
+// kernel.
 cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t ldk,
-                             const void* V, int64_t ldv, void* O, int64_t ldo, int B, int h,
-                             int T_q, int T_kv, int d, int causal, const int32_t* kv_lengths,
-                             int num_sms, int* status, cudaStream_t stream);
+                             const void* V, int64_t ldv, const void* G, int64_t ldg, void* O,
+                             int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d, int causal,
+                             const int32_t* kv_lengths, int num_sms, int* status,
+                             cudaStream_t stream);
+
+// One decode step over a bf16 KV cache (head dim 64 or 128): the T_q new query rows of
+// each batch are the last T_q of its L_b cached tokens.  ws: at least
+// decode_workspace_bytes(B, h, T_q, d) bytes of device scratch.
+size_t decode_workspace_bytes(int B, int h, int T_q, int d, int T_max);
+cudaError_t launch_decode_bf16(const void* Q, int64_t ldq, const void* Kc, int64_t ldk,
+                               const void* Vc, int64_t ldv, void* O, int64_t ldo, int B, int h,
+                               int h_kv, int T_q, int T_max, int d, const int32_t* cache_lengths,
+                               void* ws, int num_sms, int* status, cudaStream_t stream);
 
 }  // namespace mha

@@ -2,13 +2,16 @@
 // layout and the launch sequence of the forward pass.
 //
 // mha_forward (itwiki.kr "멀티 헤드 어텐션", tensor-shape table, all rows):
-//   self-attention : one GEMM  X (B*T, D) x W_qkv (D, 2h*d_k + h*d_v) -> QKV (B*T, 3D-wide)
-//                    attention reads Q, K, V as strided column views of that buffer
-//                    (the head split is addressing, not a copy) and writes Ocat (B*T, h*d_v)
-//                    GEMM  Ocat x W_o -> Y
-//   cross-attention: GEMM X_q x W_qkv[:, Q block] -> Q; GEMM X_kv x W_qkv[:, K|V blocks] -> KV
-//                    (iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", section 19),
-//                    then attention and the output GEMM as above.
+//   self-attention : one GEMM  X (B*T, D) x W_qkv (D, h*d_k + h_kv*(d_k+d_v) [+ h*d_v]) -> the
+//                    fused buffer [Q | K | V (| G)]; attention reads Q, K, V (and the gate G) as
+//                    strided column views of it (the head split is addressing, not a copy) and
+//                    writes Ocat (B*T, h*d_v); GEMM  Ocat x W_o (+ residual) -> Y
+//   cross-attention: GEMM X_q x W_qkv[:, Q block] -> Q (and X_q x W_qkv[:, G block] -> G);
+//                    GEMM X_kv x W_qkv[:, K|V blocks] -> KV (iamjaehka13.blog "[Deep Learning 5]
+//                    Attention의 내부 계산", section 19), then attention and the output GEMM.
+// Variants (itwiki.kr, section 추론 비용과 변형; iamjaehka13.blog, section 14): grouped K/V
+// heads (h_kv < h: MQA/GQA), the sigmoid output gate, the residual X' = X + O W_O, and the
+// KV-cache decode step (mha_decode).
 // All launches go to the caller's stream; nothing is allocated or synchronised here.
 #include <stdint.h>
 #include <stdlib.h>
@@ -82,20 +85,36 @@ inline bool overlaps(const void* p, size_t n, const void* q, size_t m) {
     return a < b + m && b < a + n;
 }
 
+// Column widths of the fused projection [Q | K | V | G].
+struct Widths {
+    int64_t q, k, v, g;  // h*dk, h_kv*dk, h_kv*dv, gated ? h*dv : 0
+    int64_t all() const { return q + k + v + g; }
+};
+
+Widths widths(const mha_s* m) {
+    Widths w;
+    w.q = (int64_t)m->h * m->dk;
+    w.k = (int64_t)m->h_kv * m->dk;
+    w.v = (int64_t)m->h_kv * m->dv;
+    w.g = m->gated ? (int64_t)m->h * m->dv : 0;
+    return w;
+}
+
 struct WsLayout {
     size_t q_off, kv_off, o_off, total;
 };
 
-// status | Q (B,T_q,h*dk) | KV (B,T_kv,h*(dk+dv)) | Ocat (B,T_q,h*dv).  For self-attention the
-// Q and KV regions are used as one fused (B,T,2h*dk+h*dv) buffer starting at q_off, which
-// needs no more bytes than the two regions together.
+// status | Q and G (B,T_q,h*dk [+ h*dv]) | KV (B,T_kv,h_kv*(dk+dv)) | Ocat (B,T_q,h*dv).  For
+// self-attention the Q and KV regions are used as one fused (B,T,[Q|K|V|G]) buffer starting
+// at q_off, which needs no more bytes than the two regions together.
 WsLayout ws_layout(const mha_s* m, int B, int T_q, int T_kv) {
     const size_t s = elem_bytes(m->dtype);
-    const size_t hq = (size_t)m->h * m->dk, hv = (size_t)m->h * m->dv;
+    const Widths wd = widths(m);
+    const size_t hv = (size_t)m->h * m->dv;
     WsLayout w;
     w.q_off = kStatusBytes;
-    w.kv_off = w.q_off + align256((size_t)B * T_q * hq * s);
-    w.o_off = w.kv_off + align256((size_t)B * T_kv * (hq + hv) * s);
+    w.kv_off = w.q_off + align256((size_t)B * T_q * (size_t)(wd.q + wd.g) * s);
+    w.o_off = w.kv_off + align256((size_t)B * T_kv * (size_t)(wd.k + wd.v) * s);
     w.total = w.o_off + align256((size_t)B * T_q * hv * s);
     return w;
 }
@@ -127,38 +146,40 @@ int* status_ptr(const mha_s* m) { return m->ws ? reinterpret_cast<int*>(m->ws) :
 // ---------------------------------------------------------------- step launchers (validated)
 
 mha_status run_linear(const mha_s* m, const void* A, int64_t lda, int M, int K, const void* W,
-                      int64_t ldw, int N, const void* bias, void* C, int64_t ldc,
-                      cudaStream_t stream) {
+                      int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, void* C,
+                      int64_t ldc, cudaStream_t stream) {
     cudaError_t err;
     if (m->dtype == MHA_F32) {
         err = mha::launch_gemm_f32(static_cast<const float*>(A), lda, static_cast<const float*>(W),
-                                   ldw, static_cast<const float*>(bias), static_cast<float*>(C),
-                                   ldc, M, N, K, stream);
+                                   ldw, static_cast<const float*>(bias), static_cast<const float*>(R),
+                                   ldr, static_cast<float*>(C), ldc, M, N, K, stream);
     } else {
         int sms = 0;
         const mha_status st = query_sms(&sms);
         if (st != MHA_OK) return st;
-        err = mha::launch_gemm_bf16(A, lda, W, ldw, bias, C, ldc, M, N, K, sms, status_ptr(m),
-                                    stream);
+        err = mha::launch_gemm_bf16(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, sms,
+                                    status_ptr(m), stream);
     }
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 mha_status run_attention(const mha_s* m, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
-                         const void* K, int64_t ldk, const void* V, int64_t ldv, int causal,
-                         const int32_t* kv_lengths, void* O, int64_t ldo, cudaStream_t stream) {
+                         const void* K, int64_t ldk, const void* V, int64_t ldv, const void* G,
+                         int64_t ldg, int causal, const int32_t* kv_lengths, void* O, int64_t ldo,
+                         cudaStream_t stream) {
     cudaError_t err;
     if (m->dtype == MHA_F32) {
         err = mha::launch_attn_f32(static_cast<const float*>(Q), ldq, static_cast<const float*>(K),
-                                   ldk, static_cast<const float*>(V), ldv, static_cast<float*>(O),
-                                   ldo, B, m->h, T_q, T_kv, m->dk, m->dv, causal, kv_lengths,
+                                   ldk, static_cast<const float*>(V), ldv,
+                                   static_cast<const float*>(G), ldg, static_cast<float*>(O), ldo, B,
+                                   m->h, m->h_kv, T_q, T_kv, m->dk, m->dv, causal, 0, kv_lengths,
                                    status_ptr(m), stream);
     } else {
         int sms = 0;
         const mha_status st = query_sms(&sms);
         if (st != MHA_OK) return st;
-        err = mha::launch_attn_bf16(Q, ldq, K, ldk, V, ldv, O, ldo, B, m->h, T_q, T_kv, m->dk,
-                                    causal, kv_lengths, sms, status_ptr(m), stream);
+        err = mha::launch_attn_bf16(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, m->h, m->h_kv, T_q, T_kv,
+                                    m->dk, causal, kv_lengths, sms, status_ptr(m), stream);
     }
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -184,21 +205,31 @@ mha_status check_attention_shape(const mha_s* m, int B, int T_q, int T_kv, int c
 
 extern "C" {
 
-mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype) {
+mha_status mha_create_ex(mha_t* out, int D, int h, int h_kv, int d_k, int d_v, int gated,
+                         mha_dtype dtype) {
     if (out == nullptr) return MHA_ERR_INVALID_ARG;
     *out = nullptr;
     if (D <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
+    if (h_kv <= 0 || h_kv > h || h % h_kv != 0) return MHA_ERR_INVALID_ARG;
+    if (gated != 0 && gated != 1) return MHA_ERR_INVALID_ARG;
     if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_INVALID_ARG;
-    if ((int64_t)h * (2 * (int64_t)d_k + d_v) > INT32_MAX) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)h * d_k + (int64_t)h_kv * (d_k + d_v) + (int64_t)gated * h * d_v > INT32_MAX)
+        return MHA_ERR_INVALID_ARG;
     mha_s* m = static_cast<mha_s*>(calloc(1, sizeof(mha_s)));
     if (m == nullptr) return MHA_ERR_INVALID_ARG;
     m->D = D;
     m->h = h;
+    m->h_kv = h_kv;
     m->dk = d_k;
     m->dv = d_v;
+    m->gated = gated;
     m->dtype = dtype;
     *out = m;
     return MHA_OK;
+}
+
+mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtype) {
+    return mha_create_ex(out, D, h, h, d_k, d_v, 0, dtype);
 }
 
 void mha_destroy(mha_t handle) { free(handle); }
@@ -239,33 +270,43 @@ mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, co
     if (overlaps(C, ((size_t)(M - 1) * ldc + N) * s, A, ((size_t)(M - 1) * lda + K) * s) ||
         overlaps(C, ((size_t)(M - 1) * ldc + N) * s, W, ((size_t)(K - 1) * ldw + N) * s))
         return MHA_ERR_INVALID_ARG;
-    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc,
+    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc,
                       static_cast<cudaStream_t>(stream));
 }
 
-mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
-                         const void* K, int64_t ldk, const void* V, int64_t ldv, int causal,
-                         const int32_t* kv_lengths, void* O, int64_t ldo, void* stream) {
+mha_status mha_attention_ex(mha_t handle, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
+                            const void* K, int64_t ldk, const void* V, int64_t ldv, const void* G,
+                            int64_t ldg, int causal, const int32_t* kv_lengths, void* O, int64_t ldo,
+                            void* stream) {
     if (handle == nullptr) return MHA_ERR_INVALID_ARG;
     mha_status st = check_attention_shape(handle, B, T_q, T_kv, causal);
     if (st != MHA_OK) return st;
     if (B == 0 || T_q == 0) return MHA_OK;
     if (T_kv == 0) return MHA_ERR_INVALID_ARG;
     if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return MHA_ERR_INVALID_ARG;
-    const int64_t hq = (int64_t)handle->h * handle->dk, hv = (int64_t)handle->h * handle->dv;
-    if (ldq < hq || ldk < hq || ldv < hv || ldo < hv) return MHA_ERR_INVALID_ARG;
+    const Widths wd = widths(handle);
+    const int64_t hv = (int64_t)handle->h * handle->dv;
+    if (ldq < wd.q || ldk < wd.k || ldv < wd.v || ldo < hv || (G && ldg < hv)) return MHA_ERR_INVALID_ARG;
     if (handle->dtype == MHA_BF16) {
-        if ((ldq % 8) || (ldk % 8) || (ldv % 8) || (ldo % 8)) return MHA_ERR_INVALID_ARG;
-        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        if ((ldq % 8) || (ldk % 8) || (ldv % 8) || (ldo % 8) || (G && (ldg % 8))) return MHA_ERR_INVALID_ARG;
+        if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (G && !aligned16(G)))
             return MHA_ERR_INVALID_ARG;
     }
-    return run_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths, O, ldo,
-                         static_cast<cudaStream_t>(stream));
+    return run_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, G, G ? ldg : 0, causal, kv_lengths,
+                         O, ldo, static_cast<cudaStream_t>(stream));
 }
 
-mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
-                       const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
-                       int causal, const int32_t* kv_lengths, void* out, void* stream) {
+mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
+                         const void* K, int64_t ldk, const void* V, int64_t ldv, int causal,
+                         const int32_t* kv_lengths, void* O, int64_t ldo, void* stream) {
+    return mha_attention_ex(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, nullptr, 0, causal,
+                            kv_lengths, O, ldo, stream);
+}
+
+mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                          const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                          int causal, const int32_t* kv_lengths, const void* residual, void* out,
+                          void* stream) {
     if (handle == nullptr) return MHA_ERR_INVALID_ARG;
     const mha_s* m = handle;
     const bool self = (X_kv == nullptr || X_kv == X_q);
@@ -279,18 +320,23 @@ mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, i
     if (m->dtype == MHA_BF16) {
         if (!aligned16(X_q) || (X_kv && !aligned16(X_kv)) || !aligned16(W_qkv) ||
             !aligned16(W_o) || !aligned16(out) || (b_qkv && !aligned16(b_qkv)) ||
-            (b_o && !aligned16(b_o)))
+            (b_o && !aligned16(b_o)) || (residual && !aligned16(residual)))
             return MHA_ERR_INVALID_ARG;
     }
     const size_t s = elem_bytes(m->dtype);
     const int64_t D = m->D;
-    const int64_t hq = (int64_t)m->h * m->dk, hv = (int64_t)m->h * m->dv;
-    const int64_t ncols = 2 * hq + hv;
+    const Widths wd = widths(m);
+    const int64_t hv = (int64_t)m->h * m->dv;
+    const int64_t ncols = wd.all();
     const size_t out_bytes = (size_t)B * T_q * D * s;
     if (overlaps(out, out_bytes, X_q, (size_t)B * T_q * D * s) ||
         (!self && overlaps(out, out_bytes, X_kv, (size_t)B * T_kv * D * s)) ||
         overlaps(out, out_bytes, W_qkv, (size_t)D * ncols * s) ||
         overlaps(out, out_bytes, W_o, (size_t)hv * D * s))
+        return MHA_ERR_INVALID_ARG;
+    // the residual is read in the output projection's epilogue, element by element before
+    // the same element of Y is written: it may be Y itself, but not partly overlap it
+    if (residual != nullptr && residual != out && overlaps(out, out_bytes, residual, out_bytes))
         return MHA_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(m, B, T_q, T_kv);
     if (m->ws == nullptr || m->ws_bytes < w.total) return MHA_ERR_WORKSPACE;
@@ -300,29 +346,91 @@ mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, i
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const uint8_t* wqkv = static_cast<const uint8_t*>(W_qkv);
     const uint8_t* bqkv = static_cast<const uint8_t*>(b_qkv);
+    const int64_t k_off = wd.q, v_off = wd.q + wd.k, g_off = wd.q + wd.k + wd.v;
 
     if (self) {
+        // one projection into [Q | K | V | G]
         void* qkv = ws + w.q_off;
-        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)ncols, b_qkv, qkv, ncols, cs);
+        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)ncols, b_qkv, nullptr, 0, qkv,
+                        ncols, cs);
         if (st != MHA_OK) return st;
         const uint8_t* base = static_cast<const uint8_t*>(qkv);
-        st = run_attention(m, B, T_q, T_kv, base, ncols, base + hq * s, ncols, base + 2 * hq * s,
-                           ncols, causal, kv_lengths, ocat, hv, cs);
+        st = run_attention(m, B, T_q, T_kv, base, ncols, base + k_off * s, ncols, base + v_off * s, ncols,
+                           m->gated ? base + g_off * s : nullptr, ncols, causal, kv_lengths, ocat, hv, cs);
         if (st != MHA_OK) return st;
     } else {
-        void* q = ws + w.q_off;
-        void* kv = ws + w.kv_off;
-        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)hq, b_qkv, q, hq, cs);
+        // query side [Q | G] from X_q, key/value side [K | V] from X_kv
+        const int64_t qg = wd.q + wd.g;
+        uint8_t* q = ws + w.q_off;
+        uint8_t* kv = ws + w.kv_off;
+        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)wd.q, b_qkv, nullptr, 0, q, qg, cs);
         if (st != MHA_OK) return st;
-        st = run_linear(m, X_kv, D, B * T_kv, (int)D, wqkv + hq * s, ncols, (int)(hq + hv),
-                        bqkv ? bqkv + hq * s : nullptr, kv, hq + hv, cs);
+        if (m->gated) {
+            st = run_linear(m, X_q, D, B * T_q, (int)D, wqkv + g_off * s, ncols, (int)wd.g,
+                            bqkv ? bqkv + g_off * s : nullptr, nullptr, 0, q + wd.q * s, qg, cs);
+            if (st != MHA_OK) return st;
+        }
+        st = run_linear(m, X_kv, D, B * T_kv, (int)D, wqkv + k_off * s, ncols, (int)(wd.k + wd.v),
+                        bqkv ? bqkv + k_off * s : nullptr, nullptr, 0, kv, wd.k + wd.v, cs);
         if (st != MHA_OK) return st;
-        const uint8_t* kvb = static_cast<const uint8_t*>(kv);
-        st = run_attention(m, B, T_q, T_kv, q, hq, kvb, hq + hv, kvb + hq * s, hq + hv, causal,
-                           kv_lengths, ocat, hv, cs);
+        st = run_attention(m, B, T_q, T_kv, q, qg, kv, wd.k + wd.v, kv + wd.k * s, wd.k + wd.v,
+                           m->gated ? q + wd.q * s : nullptr, qg, causal, kv_lengths, ocat, hv, cs);
         if (st != MHA_OK) return st;
     }
-    return run_linear(m, ocat, hv, B * T_q, (int)hv, W_o, D, (int)D, b_o, out, D, cs);
+    return run_linear(m, ocat, hv, B * T_q, (int)hv, W_o, D, (int)D, b_o, residual, D, out, D, cs);
+}
+
+mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                       const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                       int causal, const int32_t* kv_lengths, void* out, void* stream) {
+    return mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal, kv_lengths,
+                          nullptr, out, stream);
+}
+
+size_t mha_decode_workspace_size(mha_t handle, int B, int T_q, int T_max) {
+    if (handle == nullptr || B < 0 || T_q < 0 || T_max < 0) return 0;
+    size_t part = 0;
+    if (handle->dtype == MHA_BF16 && B > 0 && T_q > 0 && T_max > 0)
+        part = mha::decode_workspace_bytes(B, handle->h, T_q, handle->dk, T_max);
+    return kStatusBytes + align256(part);
+}
+
+mha_status mha_decode(mha_t handle, int B, int T_q, int T_max, const void* Q, int64_t ldq,
+                      const void* K_cache, int64_t ldk, const void* V_cache, int64_t ldv,
+                      const int32_t* cache_lengths, void* O, int64_t ldo, void* stream) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    const mha_s* m = handle;
+    if (B < 0 || T_q < 0 || T_max < 0) return MHA_ERR_INVALID_ARG;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    if (T_max == 0 || T_q > T_max || cache_lengths == nullptr) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)B * T_max > INT32_MAX || (int64_t)B * m->h * T_q > INT32_MAX) return MHA_ERR_INVALID_ARG;
+    if (Q == nullptr || K_cache == nullptr || V_cache == nullptr || O == nullptr) return MHA_ERR_INVALID_ARG;
+    const Widths wd = widths(m);
+    const int64_t hv = (int64_t)m->h * m->dv;
+    if (ldq < wd.q || ldk < wd.k || ldv < wd.v || ldo < hv) return MHA_ERR_INVALID_ARG;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (m->dtype == MHA_F32) {
+        if (m->dk > 256 || m->dv > 256) return MHA_ERR_UNSUPPORTED;
+        if ((T_q + 15) / 16 > 65535) return MHA_ERR_UNSUPPORTED;
+        const cudaError_t err = mha::launch_attn_f32(
+            static_cast<const float*>(Q), ldq, static_cast<const float*>(K_cache), ldk,
+            static_cast<const float*>(V_cache), ldv, nullptr, 0, static_cast<float*>(O), ldo, B, m->h,
+            m->h_kv, T_q, T_max, m->dk, m->dv, 0, 1, cache_lengths, status_ptr(m), cs);
+        return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+    }
+    if (!bf16_shape_supported(m)) return MHA_ERR_UNSUPPORTED;
+    if ((ldq % 8) || (ldk % 8) || (ldv % 8) || (ldo % 8)) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(O))
+        return MHA_ERR_INVALID_ARG;
+    const size_t need = mha_decode_workspace_size(handle, B, T_q, T_max);
+    if (m->ws == nullptr || m->ws_bytes < need) return MHA_ERR_WORKSPACE;
+    int sms = 0;
+    const mha_status st = query_sms(&sms);
+    if (st != MHA_OK) return st;
+    const cudaError_t err = mha::launch_decode_bf16(
+        Q, ldq, K_cache, ldk, V_cache, ldv, O, ldo, B, m->h, m->h_kv, T_q, T_max, m->dk, cache_lengths,
+        static_cast<uint8_t*>(m->ws) + kStatusBytes, sms, status_ptr(m), cs);
+    return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream) {

@@ -1,10 +1,14 @@
 // simt_f32.cu -- the fp32 path on CUDA cores (FFMA), for layers stored in fp32.
 // fp32 results must agree with the exact result to about 1e-5 relative; TF32 tensor cores
 // (10-bit mantissa) cannot, so both steps run in full fp32:
-//   gemm_f32_kernel  C = A W + bias   (itwiki.kr "멀티 헤드 어텐션", table rows 투영, 출력 투영)
+//   gemm_f32_kernel  C = A W + bias (+ R)   (itwiki.kr "멀티 헤드 어텐션", table rows 투영,
+//                    출력 투영; the residual R of iamjaehka13.blog "[Deep Learning 5]
+//                    Attention의 내부 계산", section 14)
 //   attn_f32_kernel  online-softmax attention for every head, any d_k, d_v <= 256, written
 //                    into the Concat layout (same page, 수식 and the shape table;
-//                    iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", sections 9-10)
+//                    iamjaehka13.blog sections 9-10), with grouped K/V heads and the sigmoid
+//                    output gate (itwiki.kr, 추론 비용과 변형), and a decode mode in which
+//                    the T_q rows are the last T_q of the L_b keys (a KV-cache step)
 #include <math.h>
 
 #include "internal.h"
@@ -19,8 +23,8 @@ constexpr int F_BM = 64, F_BN = 64, F_BK = 16;
 // order (k = 0, 1, ...) with one FFMA per product.
 __global__ void __launch_bounds__(256)
     gemm_f32_kernel(const float* __restrict__ A, int64_t lda, const float* __restrict__ W,
-                    int64_t ldw, const float* __restrict__ bias, float* __restrict__ C,
-                    int64_t ldc, int M, int N, int K) {
+                    int64_t ldw, const float* __restrict__ bias, const float* R, int64_t ldr,
+                    float* C, int64_t ldc, int M, int N, int K) {
     __shared__ float As[F_BK][F_BM + 4];  // As[k][m]
     __shared__ float Ws[F_BK][F_BN + 4];  // Ws[k][n]
     const int tx = threadIdx.x & 15;
@@ -66,7 +70,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int gn = n0 + tx * 4 + j;
-            if (gn < N) C[(int64_t)gm * ldc + gn] = acc[i][j] + (bias ? bias[gn] : 0.f);
+            if (gn < N)
+                C[(int64_t)gm * ldc + gn] =
+                    acc[i][j] + (bias ? bias[gn] : 0.f) + (R ? R[(int64_t)gm * ldr + gn] : 0.f);
         }
     }
 }
@@ -78,11 +84,15 @@ constexpr int FA_MAXV = 8;     // d_v <= 256: up to 8 output columns per lane
 
 // One block = 16 query rows of one (batch, head).  Per key tile each lane scores one key;
 // the row maximum and sum come from warp shuffles; every lane owns d_v/32 output columns.
+// Query head `head` reads K/V head head / (h / h_kv).  G (gate pre-activations, (B, T_q)
+// rows of stride ldg, head at columns head*d_v) or nullptr.  decode: row t sees keys
+// j <= L_b - T_q + t, and L_b < T_q is invalid.
 __global__ void __launch_bounds__(FA_THREADS)
     attn_f32_kernel(const float* __restrict__ Q, int64_t ldq, const float* __restrict__ K,
-                    int64_t ldk, const float* __restrict__ V, int64_t ldv, float* __restrict__ O,
-                    int64_t ldo, int h, int T_q, int T_kv, int dk, int dv, int causal,
-                    const int32_t* __restrict__ kv_lengths, float scale, int* status) {
+                    int64_t ldk, const float* __restrict__ V, int64_t ldv,
+                    const float* __restrict__ G, int64_t ldg, float* __restrict__ O,
+                    int64_t ldo, int h, int h_kv, int T_q, int T_kv, int dk, int dv, int causal,
+                    int decode, const int32_t* __restrict__ kv_lengths, float scale, int* status) {
     extern __shared__ float fsm[];
     float* Qs = fsm;                       // [FA_BQ][dk]
     float* Ks = Qs + FA_BQ * dk;           // [FA_BKEY][dk + 1]
@@ -90,9 +100,11 @@ __global__ void __launch_bounds__(FA_THREADS)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
     const int b = bh / h, head = bh - b * h;
+    const int kvh = head / (h / h_kv);
     const int q0 = blockIdx.y * FA_BQ;
     const int L = kv_lengths ? kv_lengths[b] : T_kv;
-    const bool bad = L < 1 || L > T_kv;
+    const bool bad = L < (decode ? T_q : 1) || L > T_kv;
+    const int shift = decode ? L - T_q : 0;  // row t is token t + shift
 
     if (bad) {
         if (threadIdx.x == 0) record_status(status, kStatusBadLength);
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(FA_THREADS)
         Qs[i] = t < T_q ? Q[((int64_t)b * T_q + t) * ldq + (int64_t)head * dk + e] : 0.f;
     }
     int kv_end = L;
-    if (causal && kv_end > q0 + FA_BQ) kv_end = q0 + FA_BQ;
+    if ((causal || decode) && kv_end > q0 + FA_BQ + shift) kv_end = q0 + FA_BQ + shift;
 
     float m[4], l[4], o[4][FA_MAXV];
 #pragma unroll
@@ -124,12 +136,12 @@ __global__ void __launch_bounds__(FA_THREADS)
         for (int i = threadIdx.x; i < FA_BKEY * dk; i += FA_THREADS) {
             const int j = i / dk, e = i - (i / dk) * dk;
             const int key = kt0 + j;
-            Ks[j * (dk + 1) + e] = key < T_kv ? K[((int64_t)b * T_kv + key) * ldk + (int64_t)head * dk + e] : 0.f;
+            Ks[j * (dk + 1) + e] = key < T_kv ? K[((int64_t)b * T_kv + key) * ldk + (int64_t)kvh * dk + e] : 0.f;
         }
         for (int i = threadIdx.x; i < FA_BKEY * dv; i += FA_THREADS) {
             const int j = i / dv, e = i - (i / dv) * dv;
             const int key = kt0 + j;
-            Vs[i] = key < T_kv ? V[((int64_t)b * T_kv + key) * ldv + (int64_t)head * dv + e] : 0.f;
+            Vs[i] = key < T_kv ? V[((int64_t)b * T_kv + key) * ldv + (int64_t)kvh * dv + e] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -138,7 +150,7 @@ __global__ void __launch_bounds__(FA_THREADS)
             const int t = q0 + r;
             if (t >= T_q) continue;  // warp-uniform
             const int key = kt0 + lane;
-            const bool visible = key < L && !(causal && key > t);
+            const bool visible = key < L && !((causal || decode) && key > t + shift);
             float s = -INFINITY;
             if (visible) {
                 float dot = 0.f;
@@ -180,7 +192,10 @@ __global__ void __launch_bounds__(FA_THREADS)
 #pragma unroll
         for (int u = 0; u < FA_MAXV; ++u) {
             const int e = lane + 32 * u;
-            if (e < dv) O[((int64_t)b * T_q + t) * ldo + (int64_t)head * dv + e] = o[rr][u] * inv;
+            if (e >= dv) continue;
+            float y = o[rr][u] * inv;
+            if (G != nullptr) y *= 1.f / (1.f + expf(-G[((int64_t)b * T_q + t) * ldg + (int64_t)head * dv + e]));
+            O[((int64_t)b * T_q + t) * ldo + (int64_t)head * dv + e] = y;
         }
     }
 }
@@ -188,26 +203,27 @@ __global__ void __launch_bounds__(FA_THREADS)
 }  // namespace
 
 cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t ldw,
-                            const float* bias, float* C, int64_t ldc, int M, int N, int K,
-                            cudaStream_t stream) {
+                            const float* bias, const float* R, int64_t ldr, float* C, int64_t ldc,
+                            int M, int N, int K, cudaStream_t stream) {
     const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + F_BM - 1) / F_BM));
-    gemm_f32_kernel<<<grid, 256, 0, stream>>>(A, lda, W, ldw, bias, C, ldc, M, N, K);
+    gemm_f32_kernel<<<grid, 256, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,
-                            const float* V, int64_t ldv, float* O, int64_t ldo, int B, int h,
-                            int T_q, int T_kv, int d_k, int d_v, int causal,
-                            const int32_t* kv_lengths, int* status, cudaStream_t stream) {
+                            const float* V, int64_t ldv, const float* G, int64_t ldg, float* O,
+                            int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d_k, int d_v,
+                            int causal, int decode, const int32_t* kv_lengths, int* status,
+                            cudaStream_t stream) {
     const size_t smem = sizeof(float) * (size_t)(FA_BQ * d_k + FA_BKEY * (d_k + 1) + FA_BKEY * d_v);
     cudaError_t err = cudaFuncSetAttribute(attn_f32_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const float scale = (float)(1.0 / sqrt((double)d_k));
     const dim3 grid((unsigned)(B * h), (unsigned)((T_q + FA_BQ - 1) / FA_BQ));
-    attn_f32_kernel<<<grid, FA_THREADS, smem, stream>>>(Q, ldq, K, ldk, V, ldv, O, ldo, h, T_q,
-                                                        T_kv, d_k, d_v, causal, kv_lengths, scale,
-                                                        status);
+    attn_f32_kernel<<<grid, FA_THREADS, smem, stream>>>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, h,
+                                                        h_kv, T_q, T_kv, d_k, d_v, causal, decode,
+                                                        kv_lengths, scale, status);
     return cudaGetLastError();
 }
 

@@ -30,19 +30,32 @@ class Mha:
     ``forward`` computes MultiHead(X_q, X_kv) = Concat(head_1..head_h) W_o + b_o
     with head_i = softmax(Q_i K_i^T / sqrt(d_k) [+ mask]) V_i, the fused
     [Q|K|V] projection X W_qkv + b_qkv feeding it (itwiki.kr "멀티 헤드 어텐션",
-    수식 and the tensor-shape table).
+    수식 and the tensor-shape table).  Variants (same page, 추론 비용과 변형):
+    ``h_kv`` K/V heads shared by groups of query heads (MQA/GQA), ``gated`` sigmoid
+    output gate (a fourth projection block [Q|K|V|G]); ``forward(residual=...)`` adds
+    a residual in the output projection; ``decode`` attends new tokens to a KV cache.
     """
 
     def __init__(self, D: int, h: int, d_k: int, d_v: Optional[int] = None,
-                 dtype: torch.dtype = torch.bfloat16, device=None):
+                 dtype: torch.dtype = torch.bfloat16, device=None, h_kv: Optional[int] = None,
+                 gated: bool = False):
         if dtype not in _DTYPES:
             raise TypeError(f"dtype must be one of {list(_DTYPES)}")
         self.D, self.h, self.d_k = D, h, d_k
         self.d_v = d_k if d_v is None else d_v
+        self.h_kv = h if h_kv is None else h_kv
+        self.gated = bool(gated)
         self.dtype = dtype
         self.device = torch.device("cuda") if device is None else torch.device(device)
-        self.handle = _lib.mha_create(D, h, d_k, self.d_v, _DTYPES[dtype])
+        self.handle = _lib.mha_create_ex(D, h, self.h_kv, d_k, self.d_v, int(self.gated),
+                                         _DTYPES[dtype])
         self._ws: Optional[torch.Tensor] = None
+
+    @property
+    def proj_width(self) -> int:
+        """Columns of the fused projection [Q | K | V (| G)]."""
+        return (self.h * self.d_k + self.h_kv * (self.d_k + self.d_v)
+                + (self.h * self.d_v if self.gated else 0))
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -54,8 +67,8 @@ class Mha:
     def workspace_size(self, B: int, T_q: int, T_kv: int) -> int:
         return _lib.mha_workspace_size(self.handle, B, T_q, T_kv)
 
-    def ensure_workspace(self, B: int, T_q: int, T_kv: int) -> torch.Tensor:
-        need = self.workspace_size(B, T_q, T_kv)
+    def ensure_workspace(self, B: int, T_q: int, T_kv: int, need: Optional[int] = None) -> torch.Tensor:
+        need = self.workspace_size(B, T_q, T_kv) if need is None else need
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
             _lib.mha_set_workspace(self.handle, self._ws.data_ptr(), self._ws.numel())
@@ -78,10 +91,11 @@ class Mha:
     def forward(self, X_q: torch.Tensor, W_qkv: torch.Tensor, b_qkv: Optional[torch.Tensor],
                 W_o: torch.Tensor, b_o: Optional[torch.Tensor], X_kv: Optional[torch.Tensor] = None,
                 causal: bool = False, kv_lengths: Optional[torch.Tensor] = None,
-                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                out: Optional[torch.Tensor] = None,
+                residual: Optional[torch.Tensor] = None) -> torch.Tensor:
         B, T_q, D = X_q.shape
         T_kv = T_q if X_kv is None else X_kv.shape[1]
-        ncols = 2 * self.h * self.d_k + self.h * self.d_v
+        ncols = self.proj_width
         self._check("X_q", X_q, (B, T_q, self.D))
         self._check("X_kv", X_kv, None if X_kv is None else (B, T_kv, self.D))
         self._check("W_qkv", W_qkv, (self.D, ncols))
@@ -94,10 +108,11 @@ class Mha:
         if out is None:
             out = torch.empty((B, T_q, self.D), dtype=self.dtype, device=X_q.device)
         self._check("out", out, (B, T_q, self.D))
+        self._check("residual", residual, None if residual is None else (B, T_q, self.D))
         self.ensure_workspace(B, T_q, T_kv)
-        _lib.mha_forward(self.handle, _ptr(X_q), _ptr(X_kv), B, T_q, T_kv, _ptr(W_qkv),
-                         _ptr(b_qkv), _ptr(W_o), _ptr(b_o), causal, _ptr(kv_lengths),
-                         _ptr(out), _stream())
+        _lib.mha_forward_ex(self.handle, _ptr(X_q), _ptr(X_kv), B, T_q, T_kv, _ptr(W_qkv),
+                            _ptr(b_qkv), _ptr(W_o), _ptr(b_o), causal, _ptr(kv_lengths),
+                            _ptr(residual), _ptr(out), _stream())
         return out
 
     __call__ = forward
@@ -120,12 +135,15 @@ class Mha:
 
     def attention(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal: bool = False,
                   kv_lengths: Optional[torch.Tensor] = None,
-                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                  out: Optional[torch.Tensor] = None,
+                  G: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Attention of all heads over (B, T, width) views whose last dim is contiguous;
-        head i uses columns [i*d, (i+1)*d).  Returns Ocat (B, T_q, h*d_v)."""
+        head i uses columns [i*d, (i+1)*d) of Q (and of the gate pre-activations G), K/V
+        head i // (h // h_kv).  Returns Ocat (B, T_q, h*d_v)."""
         B, T_q, _ = Q.shape
         T_kv = K.shape[1]
-        for name, t in (("Q", Q), ("K", K), ("V", V)):
+        views = [("Q", Q), ("K", K), ("V", V)] + ([("G", G)] if G is not None else [])
+        for name, t in views:
             if not t.is_cuda or t.dtype != self.dtype or t.stride(2) != 1 \
                     or t.stride(0) != t.shape[1] * t.stride(1):
                 raise ValueError(f"{name} must be a (B,T,*) {self.dtype} CUDA view with "
@@ -134,7 +152,30 @@ class Mha:
             out = torch.empty((B, T_q, self.h * self.d_v), dtype=self.dtype, device=Q.device)
         if kv_lengths is not None and (kv_lengths.dtype != torch.int32 or not kv_lengths.is_cuda):
             raise ValueError("kv_lengths must be a CUDA int32 tensor")
-        _lib.mha_attention(self.handle, B, T_q, T_kv, _ptr(Q), Q.stride(1), _ptr(K), K.stride(1),
-                           _ptr(V), V.stride(1), causal, _ptr(kv_lengths), _ptr(out),
-                           out.stride(1), _stream())
+        _lib.mha_attention_ex(self.handle, B, T_q, T_kv, _ptr(Q), Q.stride(1), _ptr(K), K.stride(1),
+                              _ptr(V), V.stride(1), _ptr(G), 0 if G is None else G.stride(1), causal,
+                              _ptr(kv_lengths), _ptr(out), out.stride(1), _stream())
+        return out
+
+    def decode(self, Q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor,
+               cache_lengths: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One decode step: the T_q new tokens' queries Q (B, T_q, h*d_k view) over the cache
+        K_cache (B, T_max, h_kv*d_k view), V_cache (B, T_max, h_kv*d_v view); cache_lengths
+        (int32, B) count the cached tokens including the new ones.  Returns (B, T_q, h*d_v)."""
+        B, T_q, _ = Q.shape
+        T_max = K_cache.shape[1]
+        for name, t in (("Q", Q), ("K_cache", K_cache), ("V_cache", V_cache)):
+            if not t.is_cuda or t.dtype != self.dtype or t.stride(2) != 1 \
+                    or t.stride(0) != t.shape[1] * t.stride(1):
+                raise ValueError(f"{name} must be a (B,T,*) {self.dtype} CUDA view with "
+                                 "contiguous rows and batches")
+        if cache_lengths.dtype != torch.int32 or not cache_lengths.is_cuda or cache_lengths.numel() != B:
+            raise ValueError("cache_lengths must be a CUDA int32 tensor of length B")
+        if out is None:
+            out = torch.empty((B, T_q, self.h * self.d_v), dtype=self.dtype, device=Q.device)
+        self.ensure_workspace(B, T_q, T_max,
+                              need=_lib.mha_decode_workspace_size(self.handle, B, T_q, T_max))
+        _lib.mha_decode(self.handle, B, T_q, T_max, _ptr(Q), Q.stride(1), _ptr(K_cache),
+                        K_cache.stride(1), _ptr(V_cache), V_cache.stride(1), _ptr(cache_lengths),
+                        _ptr(out), out.stride(1), _stream())
         return out

@@ -8,6 +8,7 @@ latter halved under the causal mask, per batch element.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
+  python bench.py --variant NAME           # a variant (gqa4, mqa, gated, residual, decode-*)
 
 One step = one mha_forward of the whole workload (three kernels: QKV GEMM,
 fused attention, output GEMM) on inputs already resident in HBM; L2 is flushed
@@ -381,6 +382,149 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------- variants
+
+# The variants of itwiki.kr "멀티 헤드 어텐션", 추론 비용과 변형 and the residual of
+# iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", section 14, measured on the
+# c3 layer shape (B=4, T=2048, D=1024, h=16, d=64, causal), and the KV-cache decode step on a
+# cache larger than L2.  Each prints its own JSON line; the default run prints none of them.
+VARIANTS = {
+    "residual": dict(h_kv=16, gated=False, residual=True),
+    "gqa4": dict(h_kv=4, gated=False, residual=False),
+    "mqa": dict(h_kv=1, gated=False, residual=False),
+    "gated": dict(h_kv=16, gated=True, residual=False),
+    "decode-mha": dict(decode=True, h_kv=16),
+    "decode-gqa4": dict(decode=True, h_kv=4),
+    "decode-mqa": dict(decode=True, h_kv=1),
+}
+DECODE_SHAPE = dict(B=32, T_q=1, T_max=8192, h=16, d=128)
+
+
+def _timed_steps(torch, fn, flush, K, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record()
+        fn()
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / K
+
+
+def run_variant(args):
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__ as g
+    g.build_library()
+    from transformer_head_scaled_02_gb300 import Mha
+    v = VARIANTS[args.variant]
+    pk, pk_src = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(0)
+
+    def bf(shape, seed, scale=1.0):
+        return to_device(wl.random_tensor(shape, seed, "bf16", scale), "bf16", torch)
+
+    if v.get("decode"):
+        c = DECODE_SHAPE
+        B, Tq, Tm, h, d, hkv = c["B"], c["T_q"], c["T_max"], c["h"], c["d"], v["h_kv"]
+        layer = Mha(h * d, h, d, d, dtype=torch.bfloat16, h_kv=hkv)
+        Q = bf((B, Tq, h * d), 1)
+        Kc = bf((B, Tm, hkv * d), 2)
+        Vc = bf((B, Tm, hkv * d), 3)
+        lens = torch.full((B,), Tm, dtype=torch.int32, device=dev)
+        O = torch.empty((B, Tq, h * d), dtype=torch.bfloat16, device=dev)
+        fn = lambda: layer.decode(Q, Kc, Vc, lens, out=O)  # noqa: E731
+        sampler.start()
+        ms = _timed_steps(torch, fn, flush, args.steps, args.warmup)
+        sampler.stop()
+        if layer.status() != 0:
+            raise RuntimeError("device status reports an error")
+        cache = 2.0 * B * Tm * hkv * 2 * d          # K and V cache rows read once
+        small = 2.0 * (Q.numel() + O.numel())
+        gbs = (cache + small) / (ms / 1e3) / 1e9
+        line = {"metric": "MHA decode step: KV-cache read bandwidth", "value": round(gbs, 1),
+                "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) cache and queries)",
+                "config": {"variant": args.variant, "B": B, "T_q": Tq, "T_max": Tm, "h": h, "h_kv": hkv,
+                           "d": d, "cache_lengths": "all T_max", "cache_bytes": cache,
+                           "l2": "flushed before every timed step"},
+                "roofline": {"kernel": "decode (partial + merge)", "bound": "hbm", "achieved": round(gbs, 1),
+                             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                             "peak_source": f"{pk_src} HBM copy"},
+                "gpu_launches": 2 * args.steps, "clocks": sampler.summary()}
+        print(json.dumps(line), flush=True)
+        return
+
+    B, T, D, h, d = 4, 2048, 1024, 16, 64
+    hkv, gated, resid = v["h_kv"], v["gated"], v["residual"]
+    layer = Mha(D, h, d, d, dtype=torch.bfloat16, h_kv=hkv, gated=gated)
+    width = layer.proj_width
+    X = bf((B, T, D), 1)
+    Wqkv = bf((D, width), 2, 0.02)
+    bqkv = bf((width,), 3, 0.02)
+    Wo = bf((h * d, D), 4, 0.02)
+    bo = bf((D,), 5, 0.02)
+    out = torch.empty((B, T, D), dtype=torch.bfloat16, device=dev)
+    fn = lambda: layer.forward(X, Wqkv, bqkv, Wo, bo, causal=True, out=out,  # noqa: E731
+                               residual=X if resid else None)
+    sampler.start()
+    ms = _timed_steps(torch, fn, flush, args.steps, args.warmup)
+    sampler.stop()
+    if layer.status() != 0:
+        raise RuntimeError("device status reports an error")
+    proj = 2.0 * B * T * D * width + 2.0 * B * T * h * d * D
+    attn = 2.0 * B * h * T * T * 2 * d * 0.5
+    tf = (proj + attn) / (ms / 1e3) / 1e12
+    # per-kernel durations of the same three launches, events between them
+    hq, hk, hvv = h * d, hkv * d, hkv * d
+    qkv = torch.empty((B, T, width), dtype=torch.bfloat16, device=dev)
+    ocat = torch.empty((B, T, h * d), dtype=torch.bfloat16, device=dev)
+    gview = qkv[..., hq + hk + hvv:] if gated else None
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        e = kev[k]
+        e[0].record()
+        layer.linear(X.view(-1, D), Wqkv, bqkv, out=qkv.view(-1, width))
+        e[1].record()
+        layer.attention(qkv[..., :hq], qkv[..., hq:hq + hk], qkv[..., hq + hk:hq + hk + hvv], causal=True,
+                        out=ocat, G=gview)
+        e[2].record()
+        layer.linear(ocat.view(-1, h * d), Wo, bo, out=out.view(-1, D),
+                     residual=X.view(-1, D) if resid else None)
+        e[3].record()
+    torch.cuda.synchronize()
+    names = ["qkv_proj", "attention", "out_proj"]
+    per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(args.steps))
+                  for i, n in enumerate(names)}
+    kflops = {"qkv_proj": 2.0 * B * T * D * width, "attention": attn, "out_proj": 2.0 * B * T * h * d * D}
+    top = max(per_kernel, key=per_kernel.get)
+    ach = kflops[top] / (per_kernel[top] / 1e3) / 1e12
+    roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                "peak_source": f"{pk_src} bf16 dense (burst)",
+                "per_kernel_ms": {k2: round(v2, 4) for k2, v2 in per_kernel.items()},
+                "per_kernel_frac_of_peak": {k2: round(kflops[k2] / (v2 / 1e3) / 1e12 / pk["bf16_tflops"], 4)
+                                            for k2, v2 in per_kernel.items()}}
+    line = {"metric": f"MHA forward TFLOP/s, {args.variant} variant (bf16 causal, 1×GB300)",
+            "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
+            "config": {"variant": args.variant, "B": B, "T": T, "D": D, "h": h, "h_kv": hkv, "d": d,
+                       "gated": gated, "residual": resid, "proj_width": width,
+                       "flops_per_step": proj + attn, "frac_of_peak": round(tf / pk["bf16_tflops"], 4),
+                       "l2": "flushed before every timed step"},
+            "roofline": roofline,
+            "gpu_launches": 3 * args.steps, "clocks": sampler.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -443,10 +587,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default=None,
+                    help="measure a variant (grouped heads, gate, residual, decode) instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.variant is not None:
+        run_variant(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -169,6 +169,17 @@ mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K,
                       void* C, int64_t ldc, void* stream);
 
 /*
+ * mha_linear_ex -- mha_linear plus a residual, C = A W + bias + R: the output projection of
+ * the residual form X' = X + O W_O (iamjaehka13.blog "[Deep Learning 5] Attention의 내부
+ * 계산", section 14) with the addition in the GEMM's epilogue.  R (M, N) row stride ldr, or
+ * NULL; it may be C itself with ldr == ldc (in place), but must not otherwise overlap C
+ * (MHA_ERR_INVALID_ARG).  bf16 needs ldr a multiple of 8 and R 16-byte aligned.
+ */
+mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K,
+                         const void* W, int64_t ldw, int N, const void* bias, const void* R,
+                         int64_t ldr, void* C, int64_t ldc, void* stream);
+
+/*
  * mha_attention -- the fused attention step for all heads: scores, scale,
  * mask, row softmax and weighted sum, written straight into the
  * concatenated layout (itwiki.kr "멀티 헤드 어텐션", table rows 헤드 분리

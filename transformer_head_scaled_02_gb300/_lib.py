@@ -39,6 +39,7 @@ _SIGNATURES = {
     "mha_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp]),
     "mha_forward_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
     "mha_linear": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp]),
+    "mha_linear_ex": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp, _i64, _vp]),
     "mha_attention": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i64,
                            _vp]),
     "mha_attention_ex": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp,
@@ -137,6 +138,12 @@ def mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, caus
 def mha_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc, stream, check: bool = True) -> int:
     code = load().mha_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc, stream)
     return _check("mha_linear", code) if check else code
+
+
+def mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, R, ldr, C, ldc, stream,
+                  check: bool = True) -> int:
+    code = load().mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, R, ldr, C, ldc, stream)
+    return _check("mha_linear_ex", code) if check else code
 
 
 def mha_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths, O, ldo,

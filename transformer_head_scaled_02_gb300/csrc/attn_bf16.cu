@@ -184,21 +184,18 @@ __device__ __forceinline__ float exp_tile(const float (&x)[128], uint64_t c2, fl
     return a0 + a1;
 }
 
-// The output gate of gated attention: f[i] *= sigmoid(g_i) for 8 consecutive outputs, g the
-// gate pre-activations (bf16) of this row.  sigmoid(x) = 1 / (1 + 2^(-x log2 e)).
-__device__ __forceinline__ void apply_gate8(const __nv_bfloat16* g, float (&f)[8]) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(g));
+// The output gate of gated attention: f[i] *= sigmoid(g_i) for 8 consecutive outputs, w the
+// 8 bf16 gate pre-activations of this row.  sigmoid(x) = 1 / (1 + 2^(-x log2 e)).
+__device__ __forceinline__ void apply_gate8(const uint4 w, float (&f)[8]) {
     const uint32_t gw[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xFFFF0000u);
-        f[2 * i] *= __frcp_rn(1.f + ex2_approx(-1.4426950408889634f * g0));
-        f[2 * i + 1] *= __frcp_rn(1.f + ex2_approx(-1.4426950408889634f * g1));
+        f[2 * i] *= __fdividef(1.f, 1.f + ex2_approx(-1.4426950408889634f * g0));
+        f[2 * i + 1] *= __fdividef(1.f, 1.f + ex2_approx(-1.4426950408889634f * g1));
     }
 }
 
-// GATE: the epilogue multiplies by the sigmoid gate (a separate instantiation, so that plain
-// attention carries none of its code or registers).
 template <int HD, bool GATE>
 __global__ void __launch_bounds__(A_THREADS, 1)
     attn_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -468,6 +465,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         const int qrow0 = q0 + t * C::BM;      // first row of this query tile
         const int row = qrow0 + r;             // this thread's query row
         const int n = n_t[t];
+        if constexpr (GATE)  // this row's gate pre-activations, into L2 for the epilogue
+            if (row < T_q)
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c)
+                    prefetch_l2(gate + ((int64_t)b * T_q + row) * ldg + (int64_t)head * HD + 64 * c);
         const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t sw = (uint32_t)(r & 7);
         const uint32_t sQt = sQ + t * C::Q_BYTES;
@@ -567,12 +569,18 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 l = l * alpha + rowsum;
                 m = m_new;
             }
+            // the gate pre-activations of this row, loaded while the last PV product runs
+            uint4 gv[GATE ? HD / 8 : 1];
+            if constexpr (GATE) {
+                const uint4* g4 = reinterpret_cast<const uint4*>(gate + ((int64_t)b * T_q + row) * ldg +
+                                                                 (int64_t)head * HD);
+#pragma unroll
+                for (int i = 0; i < HD / 8; ++i) gv[i] = row < T_q ? __ldg(g4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            }
             if (ok && __all_sync(0xffffffffu, mbar_wait(bar_pvdone + 8u * t, (uint32_t)(n - 1) & 1u,
                                                         abort_flag, status))) {
                 tc_fence_after();
                 const float inv = 1.f / l;
-                const __nv_bfloat16* grow =
-                    GATE && row < T_q ? gate + ((int64_t)b * T_q + row) * ldg + (int64_t)head * HD : nullptr;
                 // O / l (times the gate) as bf16 into this tile's Q buffer (idle now), in the
                 // TMA box layout
 #pragma unroll
@@ -587,8 +595,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
-                        if constexpr (GATE)
-                            if (grow != nullptr) apply_gate8(grow + cc * 32 + u4 * 8, f);
+                        if constexpr (GATE) apply_gate8(gv[cc * 4 + u4], f);
                         st_shared_v4(sQt + c * C::CHUNK + r * 128 + ((u ^ sw) << 4),
                                      pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
@@ -922,6 +929,8 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
             const D64Item it = item(r);
             const uint32_t sOut = sQ + (uint32_t)(r & 1) * D64_TILE;
             const int row = it.qrow0 + r_;
+            if constexpr (GATE)  // this row's gate pre-activations, into L2 for the epilogue
+                if (row < T_q) prefetch_l2(gate + ((int64_t)it.b * T_q + row) * ldg + (int64_t)it.head * 64);
             if (it.n == 0) {
                 // no valid key: the softmax is undefined, the rows are NaN (written once the
                 // item's Q load, which targets the same buffer, has landed)
@@ -992,14 +1001,20 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                     l = l * alpha + rowsum;
                     m = m_new;
                 }
+                // the gate pre-activations of this row, loaded while the last PV product runs
+                uint4 gv[GATE ? 8 : 1];
+                if constexpr (GATE) {
+                    const uint4* g4 = reinterpret_cast<const uint4*>(gate + ((int64_t)it.b * T_q + row) * ldg +
+                                                                     (int64_t)it.head * 64);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) gv[i] = row < T_q ? __ldg(g4 + i) : make_uint4(0u, 0u, 0u, 0u);
+                }
                 if (!ok || !__all_sync(0xffffffffu, mbar_wait(bar_pvdone, (gp - 1) & 1u, abort_flag, status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const float inv = 1.f / l;
-                const __nv_bfloat16* grow =
-                    GATE && row < T_q ? gate + ((int64_t)it.b * T_q + row) * ldg + (int64_t)it.head * 64 : nullptr;
                 // O / l (times the gate) as bf16 into the item's Q buffer (its last score MMA
                 // has completed)
 #pragma unroll
@@ -1013,8 +1028,7 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[u4 * 8 + i]) * inv;
-                        if constexpr (GATE)
-                            if (grow != nullptr) apply_gate8(grow + cc * 32 + u4 * 8, f);
+                        if constexpr (GATE) apply_gate8(gv[cc * 4 + u4], f);
                         st_shared_v4(sOut + r_ * 128 + (((uint32_t)u ^ sw) << 4),
                                      pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));

@@ -203,6 +203,18 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const int n0 = (tile / num_m) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            // the residual of this thread's row: the first 64 columns are loaded while the
+            // tile's MMAs run, each next 64 while the current ones are written out
+            const int rrow = m0 + q * 32 + lane;
+            auto load_res = [&](int c, uint4 (&dst)[8]) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[u] = rrow < M && n0 + c * 64 + u * 8 < N
+                                 ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)rrow * ldr + n0 + c * 64 + u * 8))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            };
+            uint4 rcur[RESID ? 8 : 1], rnext[RESID ? 8 : 1];
+            if constexpr (RESID) load_res(0, rcur);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
                 break;
@@ -210,6 +222,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
 #pragma unroll 1
             for (int c = 0; c < G_BN / 64; ++c) {
+                if constexpr (RESID) {
+                    if (c > 0)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) rcur[u] = rnext[u];
+                    if (c + 1 < G_BN / 64) load_res(c + 1, rnext);
+                }
                 uint32_t v[2][32];
                 tmem_ld32(t0 + c * 64, v[0]);
                 tmem_ld32(t0 + c * 64 + 32, v[1]);
@@ -225,23 +243,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
                 __syncwarp();
                 const uint32_t row = buf + (uint32_t)lane * 128u;
-                // this thread's 64 residual values (one 128-byte row segment), loaded up front
-                uint4 rres[RESID ? 8 : 1];
-                if constexpr (RESID) {
-                    const int grow = m0 + q * 32 + lane;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        rres[u] = grow < M && nc + u * 8 < N
-                                      ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)grow * ldr + nc + u * 8))
-                                      : make_uint4(0u, 0u, 0u, 0u);
-                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
                     if constexpr (RESID) {
-                        const uint32_t rw[4] = {rres[u].x, rres[u].y, rres[u].z, rres[u].w};
+                        const uint32_t rw[4] = {rcur[u].x, rcur[u].y, rcur[u].z, rcur[u].w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             x[2 * i] += __uint_as_float(rw[i] << 16);
@@ -465,6 +473,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             const int n0 = (tile / num_m) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            // the residual of this thread's row: the first 64 columns are loaded while the
+            // tile's MMAs run, each next 64 while the current ones are written out
+            const int rrow = m0 + q * 32 + lane;
+            auto load_res = [&](int c, uint4 (&dst)[8]) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[u] = rrow < M && n0 + c * 64 + u * 8 < N
+                                 ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)rrow * ldr + n0 + c * 64 + u * 8))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            };
+            uint4 rcur[RESID ? 8 : 1], rnext[RESID ? 8 : 1];
+            if constexpr (RESID) load_res(0, rcur);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
                 break;
@@ -472,6 +492,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
 #pragma unroll 1
             for (int c = 0; c < G_BN / 64; ++c) {
+                if constexpr (RESID) {
+                    if (c > 0)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) rcur[u] = rnext[u];
+                    if (c + 1 < G_BN / 64) load_res(c + 1, rnext);
+                }
                 uint32_t v[2][32];
                 tmem_ld32(t0 + c * 64, v[0]);
                 tmem_ld32(t0 + c * 64 + 32, v[1]);
@@ -493,23 +519,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();
                 const uint32_t row = buf + (uint32_t)lane * 128u;
-                // this thread's 64 residual values (one 128-byte row segment), loaded up front
-                uint4 rres[RESID ? 8 : 1];
-                if constexpr (RESID) {
-                    const int grow = m0 + q * 32 + lane;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        rres[u] = grow < M && nc + u * 8 < N
-                                      ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)grow * ldr + nc + u * 8))
-                                      : make_uint4(0u, 0u, 0u, 0u);
-                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
                     if constexpr (RESID) {
-                        const uint32_t rw[4] = {rres[u].x, rres[u].y, rres[u].z, rres[u].w};
+                        const uint32_t rw[4] = {rcur[u].x, rcur[u].y, rcur[u].z, rcur[u].w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             x[2 * i] += __uint_as_float(rw[i] << 16);

@@ -254,24 +254,36 @@ mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes) {
     return MHA_OK;
 }
 
-mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
-                      int64_t ldw, int N, const void* bias, void* C, int64_t ldc, void* stream) {
+mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
+                         int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, void* C,
+                         int64_t ldc, void* stream) {
     if (handle == nullptr) return MHA_ERR_INVALID_ARG;
     if (M < 0 || K <= 0 || N <= 0) return MHA_ERR_INVALID_ARG;
     if (M == 0) return MHA_OK;
     if (A == nullptr || W == nullptr || C == nullptr) return MHA_ERR_INVALID_ARG;
-    if (lda < K || ldw < N || ldc < N) return MHA_ERR_INVALID_ARG;
+    if (lda < K || ldw < N || ldc < N || (R && ldr < N)) return MHA_ERR_INVALID_ARG;
     if (handle->dtype == MHA_BF16) {
-        if ((K % 8) || (N % 8) || (lda % 8) || (ldw % 8) || (ldc % 8)) return MHA_ERR_INVALID_ARG;
-        if (!aligned16(A) || !aligned16(W) || !aligned16(C) || (bias && !aligned16(bias)))
+        if ((K % 8) || (N % 8) || (lda % 8) || (ldw % 8) || (ldc % 8) || (R && (ldr % 8)))
+            return MHA_ERR_INVALID_ARG;
+        if (!aligned16(A) || !aligned16(W) || !aligned16(C) || (bias && !aligned16(bias)) ||
+            (R && !aligned16(R)))
             return MHA_ERR_INVALID_ARG;
     }
     const size_t s = elem_bytes(handle->dtype);
-    if (overlaps(C, ((size_t)(M - 1) * ldc + N) * s, A, ((size_t)(M - 1) * lda + K) * s) ||
-        overlaps(C, ((size_t)(M - 1) * ldc + N) * s, W, ((size_t)(K - 1) * ldw + N) * s))
+    const size_t c_bytes = ((size_t)(M - 1) * ldc + N) * s;
+    if (overlaps(C, c_bytes, A, ((size_t)(M - 1) * lda + K) * s) ||
+        overlaps(C, c_bytes, W, ((size_t)(K - 1) * ldw + N) * s))
         return MHA_ERR_INVALID_ARG;
-    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc,
+    // the residual may be C itself (same rows), but not otherwise overlap it
+    if (R && !(R == C && ldr == ldc) && overlaps(C, c_bytes, R, ((size_t)(M - 1) * ldr + N) * s))
+        return MHA_ERR_INVALID_ARG;
+    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, R, R ? ldr : 0, C, ldc,
                       static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
+                      int64_t ldw, int N, const void* bias, void* C, int64_t ldc, void* stream) {
+    return mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc, stream);
 }
 
 mha_status mha_attention_ex(mha_t handle, int B, int T_q, int T_kv, const void* Q, int64_t ldq,

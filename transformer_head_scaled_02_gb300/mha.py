@@ -119,18 +119,22 @@ class Mha:
 
     # ------------------------------------------------------------ single steps
     def linear(self, A: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None) -> torch.Tensor:
-        """C = A W + bias for 2-D A (M, K), W (K, N) (row strides may exceed the width)."""
+               out: Optional[torch.Tensor] = None,
+               residual: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """C = A W + bias (+ residual) for 2-D A (M, K), W (K, N), residual (M, N) (row strides
+        may exceed the width)."""
         M, K = A.shape
         N = W.shape[1]
         if out is None:
             out = torch.empty((M, N), dtype=self.dtype, device=A.device)
-        for name, t in (("A", A), ("W", W), ("out", out)):
+        mats = [("A", A), ("W", W), ("out", out)] + ([("residual", residual)] if residual is not None else [])
+        for name, t in mats:
             if not t.is_cuda or t.dtype != self.dtype or t.stride(1) != 1:
                 raise ValueError(f"{name} must be a row-major {self.dtype} CUDA matrix")
         self._check("bias", bias, None if bias is None else (N,))
-        _lib.mha_linear(self.handle, _ptr(A), A.stride(0), M, K, _ptr(W), W.stride(0), N,
-                        _ptr(bias), _ptr(out), out.stride(0), _stream())
+        _lib.mha_linear_ex(self.handle, _ptr(A), A.stride(0), M, K, _ptr(W), W.stride(0), N,
+                           _ptr(bias), _ptr(residual), 0 if residual is None else residual.stride(0),
+                           _ptr(out), out.stride(0), _stream())
         return out
 
     def attention(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal: bool = False,

@@ -114,3 +114,63 @@ def test_wait_probe_rejects_bad_arguments(lib):
         assert L.mha_check_wait_timeout(hdl, 1000, None, check=False) == L.MHA_ERR_WORKSPACE
     finally:
         L.mha_destroy(hdl)
+
+
+def test_create_ex_validates_groups_and_gate(lib):
+    h = ctypes.c_void_p()
+    # h_kv must divide h and lie in [1, h]; gated is 0 or 1
+    for args in ((512, 8, 3, 64, 64, 0, 1), (512, 8, 0, 64, 64, 0, 1), (512, 8, 16, 64, 64, 0, 1),
+                 (512, 8, 8, 64, 64, 2, 1)):
+        assert lib.mha_create_ex(ctypes.byref(h), *args) == L.MHA_ERR_INVALID_ARG
+    for h_kv in (1, 2, 4, 8):
+        hdl = L.mha_create_ex(512, 8, h_kv, 64, 64, 1, L.MHA_BF16)
+        L.mha_destroy(hdl)
+
+
+def test_workspace_size_grouped_and_gated(lib):
+    # self-attention: status + [Q|G] region (B*T*(h*dk + h*dv)) + [K|V] (B*T*h_kv*(dk+dv)) + Ocat
+    B, T, D, h, h_kv, d = 2, 256, 512, 8, 2, 64
+    hdl = L.mha_create_ex(D, h, h_kv, d, d, 1, L.MHA_BF16)
+    try:
+        qg = B * T * (h * d + h * d) * 2
+        kv = B * T * h_kv * 2 * d * 2
+        oc = B * T * h * d * 2
+        assert L.mha_workspace_size(hdl, B, T, T) == 256 + qg + kv + oc
+    finally:
+        L.mha_destroy(hdl)
+
+
+def test_decode_and_linear_ex_reject_bad_arguments(lib):
+    bf = L.mha_create_ex(1024, 16, 4, 64, 64, 0, L.MHA_BF16)
+    odd = L.mha_create_ex(96, 3, 1, 32, 32, 0, L.MHA_BF16)   # d = 32: no tensor-core kernel
+    fake = 1 << 40
+    try:
+        def dec(h, **kw):
+            a = dict(B=2, T_q=1, T_max=1024, Q=fake, ldq=1024, K=fake, ldk=256, V=fake, ldv=256,
+                     lens=fake, O=fake + (1 << 30), ldo=1024)
+            a.update(kw)
+            return L.mha_decode(h, a["B"], a["T_q"], a["T_max"], a["Q"], a["ldq"], a["K"], a["ldk"],
+                                a["V"], a["ldv"], a["lens"], a["O"], a["ldo"], None, check=False)
+        assert dec(None) == L.MHA_ERR_INVALID_ARG
+        assert dec(bf, T_q=2000) == L.MHA_ERR_INVALID_ARG          # more new tokens than the cache
+        assert dec(bf, lens=None) == L.MHA_ERR_INVALID_ARG
+        assert dec(bf, ldk=128) == L.MHA_ERR_INVALID_ARG           # K row narrower than h_kv*d_k
+        assert dec(bf, Q=fake + 2) == L.MHA_ERR_INVALID_ARG        # misaligned bf16 pointer
+        assert dec(bf) == L.MHA_ERR_WORKSPACE                      # no workspace attached
+        assert dec(odd, ldq=96, ldk=32, ldv=32, ldo=96) == L.MHA_ERR_UNSUPPORTED
+        assert dec(bf, B=0) == L.MHA_OK and dec(bf, T_q=0) == L.MHA_OK
+        assert L.mha_decode_workspace_size(bf, 2, 1, 1024) > 256
+        assert L.mha_decode_workspace_size(None, 2, 1, 1024) == 0
+
+        def lin(**kw):
+            a = dict(A=fake, lda=64, M=128, K=64, W=fake + (1 << 28), ldw=64, N=64, bias=None,
+                     R=fake + (2 << 28), ldr=64, C=fake + (3 << 28), ldc=64)
+            a.update(kw)
+            return L.mha_linear_ex(bf, a["A"], a["lda"], a["M"], a["K"], a["W"], a["ldw"], a["N"],
+                                   a["bias"], a["R"], a["ldr"], a["C"], a["ldc"], None, check=False)
+        assert lin(ldr=32) == L.MHA_ERR_INVALID_ARG                 # residual row narrower than N
+        assert lin(R=fake + (3 << 28) + 2) == L.MHA_ERR_INVALID_ARG # misaligned, overlapping C
+        assert lin(R=fake + (3 << 28) + 64) == L.MHA_ERR_INVALID_ARG # partly overlaps C
+    finally:
+        L.mha_destroy(bf)
+        L.mha_destroy(odd)

@@ -40,6 +40,9 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "c3_bf16_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# batch chunks of the end-to-end (host buffers) measurement; each chunk's copies overlap the
+# other chunks' kernels
+E2E_CHUNKS = 2
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -321,14 +324,19 @@ def run_ours(args):
            for _ in range(Ke)]
     barrier(world)
     torch.cuda.synchronize()
+    e2e_chunks = min(E2E_CHUNKS, w.B)
+
+    def forward_host():
+        layer.forward_host(xh, d["W_qkv"], d["b_qkv"], d["W_o"], d["b_o"], out=yh, X_kv=xkvh,
+                           causal=w.causal, kv_lengths=kvl, chunks=e2e_chunks)
+
+    for _ in range(2):
+        forward_host()
+    torch.cuda.synchronize()
     for k in range(Ke):
         flush.zero_()
         eev[k][0].record()
-        d["X_q"].copy_(xh, non_blocking=True)
-        if xkvh is not None:
-            d["X_kv"].copy_(xkvh, non_blocking=True)
-        forward()
-        yh.copy_(out, non_blocking=True)
+        forward_host()
         eev[k][1].record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev), world, dev) / Ke
@@ -367,8 +375,9 @@ def run_ours(args):
         "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
-                "note": "mha_forward via the public API with pinned host X in and Y out; "
-                        "weights resident"},
+                "chunks": e2e_chunks,
+                "note": "mha_forward_host through the C ABI: pinned host X in and Y out, the batch "
+                        "in chunks whose host-device copies overlap the kernels; weights resident"},
         "gpu_launches": launches_per_step * K,
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(wall, 3),

@@ -31,6 +31,9 @@
  *  - Outputs must not alias inputs.
  *  - Every function is thread-compatible: one handle must not be used from
  *    two host threads at once.
+ *  - The work a handle launches must not overlap on the GPU: its workspace
+ *    (the status word and the scratch tensors) is shared by all its calls, so
+ *    issue them on one stream or order the streams with events.
  */
 #ifndef MHA_H_
 #define MHA_H_
@@ -91,8 +94,9 @@ mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtyp
 mha_status mha_create_ex(mha_t* out, int D, int h, int h_kv, int d_k, int d_v, int gated,
                          mha_dtype dtype);
 
-/* mha_destroy -- free the handle (NULL is ignored).  Does not touch the
- * caller's workspace. */
+/* mha_destroy -- free the handle and the copy streams and events mha_set_workspace
+ * created for it (NULL is ignored).  Does not touch the caller's workspace; no work
+ * of the handle may still be in flight. */
 void mha_destroy(mha_t handle);
 
 /*
@@ -109,7 +113,9 @@ size_t mha_workspace_size(mha_t handle, int B, int T_q, int T_kv);
  * mha_set_workspace -- attach caller-owned device memory (256-byte aligned,
  * `bytes` long) to the handle, and zero its status block (a synchronous
  * cudaMemset of 256 bytes).  The memory must stay valid while calls using
- * the handle are in flight.  NULL detaches.
+ * the handle are in flight.  NULL detaches.  The first attach also creates the
+ * two copy streams and the events mha_forward_host uses, on the current device
+ * (MHA_ERR_CUDA if that fails); they live until mha_destroy.
  */
 mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes);
 
@@ -155,6 +161,40 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
                           int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
                           const void* b_o, int causal, const int32_t* kv_lengths,
                           const void* residual, void* out, void* stream);
+
+/*
+ * mha_forward_host_workspace_size -- workspace bytes mha_forward_host needs: the forward's
+ * scratch (mha_workspace_size) for one chunk of ceil(B / min(chunks, B)) batch elements,
+ * then device copies of X_q (B,T_q,D), X_kv (B,T_kv,D), the residual (B,T_q,D) and Y
+ * (B,T_q,D), each 256-byte aligned.  0 for an invalid handle, a size <= 0 or chunks outside
+ * [1, 16].
+ */
+size_t mha_forward_host_workspace_size(mha_t handle, int B, int T_q, int T_kv, int chunks);
+
+/*
+ * mha_forward_host -- mha_forward_ex with the activations in HOST memory: X_q, X_kv (NULL
+ * or == X_q for self-attention), residual (NULL, == X_q, or another (B,T_q,D) buffer) and
+ * out are host pointers; W_qkv, b_qkv, W_o, b_o and kv_lengths stay device pointers
+ * (resident weights).  Host buffers should be pinned (cudaHostAlloc/cudaHostRegister) for
+ * the copies to run asynchronously.
+ * The batch is cut into min(chunks, B) chunks of whole batch elements (every batch element
+ * is an independent problem, so the result is the same as one mha_forward_ex over the
+ * whole batch, bit for bit).  Chunk c's inputs go to the device on the handle's
+ * host-to-device stream, its forward runs on `stream` once they are in, and its output
+ * goes back on the handle's device-to-host stream while chunk c+1 computes, so copies in
+ * both directions overlap the kernels.  The copies start after the work already queued on
+ * `stream`, and `stream` completes only once all of `out` has landed: synchronise on
+ * `stream` before reading `out` or reusing the host inputs.  Asynchronous; allocates
+ * nothing.
+ * Needs a workspace of mha_forward_host_workspace_size(B, T_q, T_kv, chunks) bytes attached
+ * on the current device (else MHA_ERR_WORKSPACE; another current device:
+ * MHA_ERR_INVALID_ARG).  chunks outside [1, 16] is MHA_ERR_INVALID_ARG; other arguments as
+ * for mha_forward_ex.  Launches 3 (self) or 4 (cross) kernels per chunk.
+ */
+mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q,
+                            int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                            const void* b_o, int causal, const int32_t* kv_lengths,
+                            const void* residual, void* out, int chunks, void* stream);
 
 /*
  * mha_linear -- one projection step, C = A W + bias

@@ -174,3 +174,43 @@ def test_decode_and_linear_ex_reject_bad_arguments(lib):
     finally:
         L.mha_destroy(bf)
         L.mha_destroy(odd)
+
+
+def test_forward_host_workspace_layout(lib):
+    hdl = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    try:
+        B, T, D = 4, 2048, 1024
+        act = B * T * D * 2
+        # chunk scratch (for ceil(B / chunks) batch elements) + X_q, X_kv, residual, Y copies
+        for chunks, Bc in ((1, 4), (2, 2), (3, 2), (4, 1), (16, 1)):
+            assert L.mha_forward_host_workspace_size(hdl, B, T, T, chunks) == \
+                L.mha_workspace_size(hdl, Bc, T, T) + 4 * act
+        assert L.mha_forward_host_workspace_size(hdl, B, T, T, 0) == 0
+        assert L.mha_forward_host_workspace_size(hdl, B, T, T, 17) == 0
+        assert L.mha_forward_host_workspace_size(hdl, 0, T, T, 1) == 0
+        assert L.mha_forward_host_workspace_size(None, B, T, T, 1) == 0
+    finally:
+        L.mha_destroy(hdl)
+
+
+def test_forward_host_rejects_bad_arguments_before_any_copy(lib):
+    hdl = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    fake = 1 << 40  # never dereferenced: every call below is rejected first
+    try:
+        def fwd(**kw):
+            a = dict(X_q=fake, X_kv=None, B=2, T_q=128, T_kv=128, W_qkv=fake, b_qkv=None,
+                     W_o=fake, b_o=None, causal=0, kv_lengths=None, residual=None,
+                     out=fake + (1 << 30), chunks=2, stream=None)
+            a.update(kw)
+            return L.mha_forward_host(hdl, check=False, **a)
+        assert L.mha_forward_host(None, fake, None, 2, 128, 128, fake, None, fake, None, 0, None,
+                                  None, fake, 2, None, check=False) == L.MHA_ERR_INVALID_ARG
+        assert fwd(chunks=0) == L.MHA_ERR_INVALID_ARG
+        assert fwd(chunks=17) == L.MHA_ERR_INVALID_ARG
+        assert fwd(T_kv=64) == L.MHA_ERR_INVALID_ARG           # self-attention needs T_kv == T_q
+        assert fwd(out=fake) == L.MHA_ERR_INVALID_ARG          # out aliases X_q
+        assert fwd(W_qkv=None) == L.MHA_ERR_INVALID_ARG
+        assert fwd(B=0) == L.MHA_OK                            # empty batch: nothing to do
+        assert fwd() == L.MHA_ERR_WORKSPACE                    # no workspace attached
+    finally:
+        L.mha_destroy(hdl)

@@ -38,6 +38,9 @@ _SIGNATURES = {
     "mha_set_workspace": (_i, [_vp, _vp, _sz]),
     "mha_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp]),
     "mha_forward_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
+    "mha_forward_host_workspace_size": (_sz, [_vp, _i, _i, _i, _i]),
+    "mha_forward_host": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i,
+                              _vp]),
     "mha_linear": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp]),
     "mha_linear_ex": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp, _i64, _vp]),
     "mha_attention": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i64,
@@ -133,6 +136,17 @@ def mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, caus
     code = load().mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o,
                                  int(causal), kv_lengths, residual, out, stream)
     return _check("mha_forward_ex", code) if check else code
+
+
+def mha_forward_host_workspace_size(handle, B, T_q, T_kv, chunks) -> int:
+    return load().mha_forward_host_workspace_size(handle, B, T_q, T_kv, chunks)
+
+
+def mha_forward_host(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal, kv_lengths,
+                     residual, out, chunks, stream, check: bool = True) -> int:
+    code = load().mha_forward_host(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o,
+                                   int(causal), kv_lengths, residual, out, chunks, stream)
+    return _check("mha_forward_host", code) if check else code
 
 
 def mha_linear(handle, A, lda, M, K, W, ldw, N, bias, C, ldc, stream, check: bool = True) -> int:

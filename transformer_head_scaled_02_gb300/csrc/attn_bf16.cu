@@ -614,6 +614,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         }
     }
 
+    // lanes that skipped a one-thread role wait here for it: the CTA barrier below must
+    // see whole warps, or it can complete while a role is still running
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -1042,6 +1045,9 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
         }
     }
 
+    // lanes that skipped a one-thread role wait here for it: the CTA barrier below must
+    // see whole warps, or it can complete while a role is still running
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

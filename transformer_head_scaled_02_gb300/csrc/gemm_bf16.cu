@@ -282,6 +282,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         __syncwarp();
     }
 
+    // lanes that skipped a one-thread role wait here for it: the CTA barrier below must
+    // see whole warps, or it can complete while a role is still running
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -558,6 +561,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         __syncwarp();
     }
 
+    // lanes that skipped a one-thread role wait here for it: the CTA barrier below must
+    // see whole warps, or it can complete while a role is still running
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // neither CTA leaves while the pair's MMAs may touch its memory

@@ -12,11 +12,17 @@
 // The opaque handle of include/mha.h: the layer configuration and the caller's workspace.
 // h_kv: K/V heads (h for plain multi-head attention, 1 for MQA); gated: the fused projection
 // carries a fourth block of h*d_v gate pre-activations.
+// aux_*: the two copy streams and the events of mha_forward_host, created with the first
+// workspace on the device that was current then (aux_dev; -1: none yet).
+constexpr int kHostMaxChunks = 16;
 struct mha_s {
     int D, h, h_kv, dk, dv, gated;
     mha_dtype dtype;
     void* ws;
     size_t ws_bytes;
+    int aux_dev;
+    cudaStream_t aux_h2d, aux_d2h;
+    cudaEvent_t aux_start, aux_done, aux_in[kHostMaxChunks], aux_out[kHostMaxChunks];
 };
 
 namespace mha {

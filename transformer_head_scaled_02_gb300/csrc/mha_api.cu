@@ -201,6 +201,47 @@ mha_status check_attention_shape(const mha_s* m, int B, int T_q, int T_kv, int c
     return MHA_OK;
 }
 
+// The copy streams and events of mha_forward_host, on the current device.  All or none.
+mha_status create_aux(mha_s* m) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+    mha_s t = *m;
+    bool ok = cudaStreamCreateWithFlags(&t.aux_h2d, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamCreateWithFlags(&t.aux_d2h, cudaStreamNonBlocking) == cudaSuccess;
+    const unsigned fl = cudaEventDisableTiming;
+    ok = ok && cudaEventCreateWithFlags(&t.aux_start, fl) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&t.aux_done, fl) == cudaSuccess;
+    for (int i = 0; ok && i < kHostMaxChunks; ++i)
+        ok = cudaEventCreateWithFlags(&t.aux_in[i], fl) == cudaSuccess &&
+             cudaEventCreateWithFlags(&t.aux_out[i], fl) == cudaSuccess;
+    if (!ok) return MHA_ERR_CUDA;  // (a partial set is left to the process teardown)
+    t.aux_dev = dev;
+    *m = t;
+    return MHA_OK;
+}
+
+// mha_forward_host: the forward's scratch for one chunk of Bc batch elements, then device
+// copies of X_q, X_kv, the residual and Y for the whole batch.
+struct HostLayout {
+    int chunks, Bc;
+    size_t x_off, xkv_off, r_off, y_off, total;
+};
+
+bool host_layout(const mha_s* m, int B, int T_q, int T_kv, int chunks, HostLayout* L) {
+    if (B <= 0 || T_q <= 0 || T_kv <= 0 || chunks < 1 || chunks > kHostMaxChunks) return false;
+    const int c = chunks < B ? chunks : B;
+    L->Bc = (B + c - 1) / c;
+    L->chunks = (B + L->Bc - 1) / L->Bc;
+    const size_t s = elem_bytes(m->dtype);
+    const size_t xq = (size_t)B * T_q * (size_t)m->D * s, xkv = (size_t)B * T_kv * (size_t)m->D * s;
+    L->x_off = align256(ws_layout(m, L->Bc, T_q, T_kv).total);
+    L->xkv_off = L->x_off + align256(xq);
+    L->r_off = L->xkv_off + align256(xkv);
+    L->y_off = L->r_off + align256(xq);
+    L->total = L->y_off + align256(xq);
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -224,6 +265,7 @@ mha_status mha_create_ex(mha_t* out, int D, int h, int h_kv, int d_k, int d_v, i
     m->dv = d_v;
     m->gated = gated;
     m->dtype = dtype;
+    m->aux_dev = -1;
     *out = m;
     return MHA_OK;
 }
@@ -232,7 +274,24 @@ mha_status mha_create(mha_t* out, int D, int h, int d_k, int d_v, mha_dtype dtyp
     return mha_create_ex(out, D, h, h, d_k, d_v, 0, dtype);
 }
 
-void mha_destroy(mha_t handle) { free(handle); }
+void mha_destroy(mha_t handle) {
+    if (handle == nullptr) return;
+    if (handle->aux_dev >= 0) {
+        int cur = 0;
+        const bool swap = cudaGetDevice(&cur) == cudaSuccess && cur != handle->aux_dev &&
+                          cudaSetDevice(handle->aux_dev) == cudaSuccess;
+        cudaStreamDestroy(handle->aux_h2d);
+        cudaStreamDestroy(handle->aux_d2h);
+        cudaEventDestroy(handle->aux_start);
+        cudaEventDestroy(handle->aux_done);
+        for (int i = 0; i < kHostMaxChunks; ++i) {
+            cudaEventDestroy(handle->aux_in[i]);
+            cudaEventDestroy(handle->aux_out[i]);
+        }
+        if (swap) cudaSetDevice(cur);
+    }
+    free(handle);
+}
 
 size_t mha_workspace_size(mha_t handle, int B, int T_q, int T_kv) {
     if (handle == nullptr || B < 0 || T_q < 0 || T_kv < 0) return 0;
@@ -249,6 +308,10 @@ mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes) {
     if ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) != 0 || bytes < kStatusBytes)
         return MHA_ERR_INVALID_ARG;
     if (cudaMemset(dev_ptr, 0, kStatusBytes) != cudaSuccess) return MHA_ERR_CUDA;
+    if (handle->aux_dev < 0) {
+        const mha_status st = create_aux(handle);
+        if (st != MHA_OK) return st;
+    }
     handle->ws = dev_ptr;
     handle->ws_bytes = bytes;
     return MHA_OK;
@@ -443,6 +506,91 @@ mha_status mha_decode(mha_t handle, int B, int T_q, int T_max, const void* Q, in
         Q, ldq, K_cache, ldk, V_cache, ldv, O, ldo, B, m->h, m->h_kv, T_q, T_max, m->dk, cache_lengths,
         static_cast<uint8_t*>(m->ws) + kStatusBytes, sms, status_ptr(m), cs);
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+size_t mha_forward_host_workspace_size(mha_t handle, int B, int T_q, int T_kv, int chunks) {
+    HostLayout L;
+    if (handle == nullptr || !host_layout(handle, B, T_q, T_kv, chunks, &L)) return 0;
+    return L.total;
+}
+
+mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                            const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                            int causal, const int32_t* kv_lengths, const void* residual, void* out,
+                            int chunks, void* stream) {
+    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
+    mha_s* m = handle;
+    const bool self = (X_kv == nullptr || X_kv == X_q);
+    if (self && T_kv != T_q) return MHA_ERR_INVALID_ARG;
+    if (chunks < 1 || chunks > kHostMaxChunks) return MHA_ERR_INVALID_ARG;
+    mha_status st = check_attention_shape(m, B, T_q, T_kv, causal);
+    if (st != MHA_OK) return st;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    if (T_kv == 0) return MHA_ERR_INVALID_ARG;
+    if (X_q == nullptr || W_qkv == nullptr || W_o == nullptr || out == nullptr) return MHA_ERR_INVALID_ARG;
+    const size_t s = elem_bytes(m->dtype);
+    const size_t row_q = (size_t)m->D * s;
+    if (overlaps(out, (size_t)B * T_q * row_q, X_q, (size_t)B * T_q * row_q) ||
+        (!self && overlaps(out, (size_t)B * T_q * row_q, X_kv, (size_t)B * T_kv * row_q)) ||
+        (residual != nullptr && residual != X_q &&
+         overlaps(out, (size_t)B * T_q * row_q, residual, (size_t)B * T_q * row_q)))
+        return MHA_ERR_INVALID_ARG;
+    HostLayout L;
+    if (!host_layout(m, B, T_q, T_kv, chunks, &L)) return MHA_ERR_INVALID_ARG;
+    if (m->ws == nullptr || m->ws_bytes < L.total || m->aux_dev < 0) return MHA_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+    if (dev != m->aux_dev) return MHA_ERR_INVALID_ARG;
+
+    uint8_t* ws = static_cast<uint8_t*>(m->ws);
+    uint8_t* xd = ws + L.x_off;
+    uint8_t* xkvd = ws + L.xkv_off;
+    uint8_t* rd = residual == nullptr ? nullptr : residual == X_q ? xd : ws + L.r_off;
+    uint8_t* yd = ws + L.y_off;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    auto cuda = [](cudaError_t e) { return e == cudaSuccess; };
+    // the copies start after the work already queued on the caller's stream
+    if (!cuda(cudaEventRecord(m->aux_start, cs)) || !cuda(cudaStreamWaitEvent(m->aux_h2d, m->aux_start, 0)) ||
+        !cuda(cudaStreamWaitEvent(m->aux_d2h, m->aux_start, 0)))
+        return MHA_ERR_CUDA;
+    // inputs, chunk by chunk, on the host-to-device stream
+    for (int c = 0; c < L.chunks; ++c) {
+        const int b0 = c * L.Bc, nb = (B - b0) < L.Bc ? (B - b0) : L.Bc;
+        const size_t oq = (size_t)b0 * T_q * row_q, nq = (size_t)nb * T_q * row_q;
+        if (!cuda(cudaMemcpyAsync(xd + oq, static_cast<const uint8_t*>(X_q) + oq, nq, cudaMemcpyHostToDevice,
+                                  m->aux_h2d)))
+            return MHA_ERR_CUDA;
+        if (!self) {
+            const size_t okv = (size_t)b0 * T_kv * row_q, nkv = (size_t)nb * T_kv * row_q;
+            if (!cuda(cudaMemcpyAsync(xkvd + okv, static_cast<const uint8_t*>(X_kv) + okv, nkv,
+                                      cudaMemcpyHostToDevice, m->aux_h2d)))
+                return MHA_ERR_CUDA;
+        }
+        if (rd != nullptr && rd != xd &&
+            !cuda(cudaMemcpyAsync(rd + oq, static_cast<const uint8_t*>(residual) + oq, nq,
+                                  cudaMemcpyHostToDevice, m->aux_h2d)))
+            return MHA_ERR_CUDA;
+        if (!cuda(cudaEventRecord(m->aux_in[c], m->aux_h2d))) return MHA_ERR_CUDA;
+    }
+    // each chunk's forward on the caller's stream once its inputs are in; its output back on
+    // the device-to-host stream while the next chunk computes
+    for (int c = 0; c < L.chunks; ++c) {
+        const int b0 = c * L.Bc, nb = (B - b0) < L.Bc ? (B - b0) : L.Bc;
+        const size_t oq = (size_t)b0 * T_q * row_q, nq = (size_t)nb * T_q * row_q;
+        if (!cuda(cudaStreamWaitEvent(cs, m->aux_in[c], 0))) return MHA_ERR_CUDA;
+        st = mha_forward_ex(m, xd + oq, self ? nullptr : xkvd + (size_t)b0 * T_kv * row_q, nb, T_q, T_kv,
+                            W_qkv, b_qkv, W_o, b_o, causal, kv_lengths == nullptr ? nullptr : kv_lengths + b0,
+                            rd == nullptr ? nullptr : rd + oq, yd + oq, stream);
+        if (st != MHA_OK) return st;
+        if (!cuda(cudaEventRecord(m->aux_out[c], cs)) || !cuda(cudaStreamWaitEvent(m->aux_d2h, m->aux_out[c], 0)) ||
+            !cuda(cudaMemcpyAsync(static_cast<uint8_t*>(out) + oq, yd + oq, nq, cudaMemcpyDeviceToHost,
+                                  m->aux_d2h)))
+            return MHA_ERR_CUDA;
+    }
+    // the caller's stream completes only after the last output has landed in host memory
+    if (!cuda(cudaEventRecord(m->aux_done, m->aux_d2h)) || !cuda(cudaStreamWaitEvent(cs, m->aux_done, 0)))
+        return MHA_ERR_CUDA;
+    return MHA_OK;
 }
 
 mha_status mha_get_status(mha_t handle, int32_t* status_out, void* stream) {

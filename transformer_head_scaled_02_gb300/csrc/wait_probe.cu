@@ -22,6 +22,7 @@ __global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
     }
     __syncthreads();
     if ((threadIdx.x & 31) == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+    __syncwarp();  // whole warps reach the CTA barrier
     __syncthreads();
 }
 

@@ -117,6 +117,39 @@ class Mha:
 
     __call__ = forward
 
+    def forward_host(self, X_q: torch.Tensor, W_qkv: torch.Tensor, b_qkv: Optional[torch.Tensor],
+                     W_o: torch.Tensor, b_o: Optional[torch.Tensor], out: torch.Tensor,
+                     X_kv: Optional[torch.Tensor] = None, causal: bool = False,
+                     kv_lengths: Optional[torch.Tensor] = None,
+                     residual: Optional[torch.Tensor] = None, chunks: int = 4) -> torch.Tensor:
+        """forward() with X_q, X_kv, residual and out in (pinned) host memory and the weights on
+        the device: the batch goes through in chunks whose copies overlap the kernels.  Enqueued
+        on the current stream; synchronise it before reading ``out``."""
+        B, T_q, D = X_q.shape
+        T_kv = T_q if X_kv is None else X_kv.shape[1]
+        for name, t, T in (("X_q", X_q, T_q), ("X_kv", X_kv, T_kv), ("residual", residual, T_q),
+                           ("out", out, T_q)):
+            if t is None:
+                continue
+            if t.is_cuda or t.dtype != self.dtype or not t.is_contiguous() or tuple(t.shape) != (B, T, self.D):
+                raise ValueError(f"{name} must be a contiguous host {self.dtype} tensor of shape "
+                                 f"{(B, T, self.D)}")
+        self._check("W_qkv", W_qkv, (self.D, self.proj_width))
+        self._check("b_qkv", b_qkv, None if b_qkv is None else (self.proj_width,))
+        self._check("W_o", W_o, (self.h * self.d_v, self.D))
+        self._check("b_o", b_o, None if b_o is None else (self.D,))
+        if kv_lengths is not None and (kv_lengths.dtype != torch.int32 or not kv_lengths.is_cuda
+                                       or kv_lengths.numel() != B):
+            raise ValueError("kv_lengths must be a CUDA int32 tensor of length B")
+        need = _lib.mha_forward_host_workspace_size(self.handle, B, T_q, T_kv, chunks)
+        if need == 0:
+            raise ValueError("invalid size or chunk count")
+        self.ensure_workspace(B, T_q, T_kv, need=need)
+        _lib.mha_forward_host(self.handle, _ptr(X_q), _ptr(X_kv), B, T_q, T_kv, _ptr(W_qkv),
+                              _ptr(b_qkv), _ptr(W_o), _ptr(b_o), causal, _ptr(kv_lengths),
+                              _ptr(residual), _ptr(out), chunks, _stream())
+        return out
+
     # ------------------------------------------------------------ single steps
     def linear(self, A: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor] = None,
                out: Optional[torch.Tensor] = None,

@@ -184,6 +184,26 @@ __device__ __forceinline__ float exp_tile(const float (&x)[128], uint64_t c2, fl
     return a0 + a1;
 }
 
+// p = 2^(s*c + neg) for the 64 scores [64 h, 64 h + 64) of a row; returns their sum and
+// writes P as packed bf16 pairs.
+__device__ __forceinline__ float exp_half(const float (&x)[128], int h, uint64_t c2, float neg,
+                                          uint32_t (&pk)[32]) {
+    const uint64_t neg2 = pack2(neg, neg);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        float a0, a1;
+        unpack2(fma2(pack2(x[64 * h + 2 * k], x[64 * h + 2 * k + 1]), c2, neg2), a0, a1);
+        const float y0 = ex2_approx(a0), y1 = ex2_approx(a1);
+        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
+        pk[k] = pack_bf16x2(y0, y1);
+    }
+    const uint64_t s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+    float a0, a1;
+    unpack2(add2(s01, s23), a0, a1);
+    return a0 + a1;
+}
+
 // The output gate of gated attention: f[i] *= sigmoid(g_i) for 8 consecutive outputs, w the
 // 8 bf16 gate pre-activations of this row.  sigmoid(x) = 1 / (1 + 2^(-x log2 e)).
 __device__ __forceinline__ void apply_gate8(const uint4 w, float (&f)[8]) {
@@ -963,46 +983,58 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
                     tc_fence_before();
                     mbar_arrive(bar_sfree);
                     ++gs;
-                    // the reference moves only when it would otherwise let P exceed 2^32
-                    const float m_tile = row_max(x) * scale_log2;
-                    const float m_new = m_tile > m + 32.0f ? m_tile : m;
-                    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
-                    uint32_t pk[64];
-                    const float rowsum = exp_tile(x, pack2(scale_log2, scale_log2),
-                                                  m_new == -INFINITY ? 0.f : -m_new, pk);
-                    if (j > 0) {
+                    // P against the current reference m, each half stored to TMEM as soon as it
+                    // is computed; any reference gives the same O / l, it only has to keep P
+                    // finite.  The first tile, or any tile where some row's sum would exceed
+                    // 2^64, takes the exact row maximum as the new reference instead (and
+                    // rescales O); the P stores of the fast attempt are simply overwritten.
+                    const uint64_t c2 = pack2(scale_log2, scale_log2);
+                    float rowsum = 0.f, alpha = 1.f;
+                    bool slow = j == 0;
+                    if (!slow) {
+                        uint32_t pk[32];
+                        rowsum = exp_half(x, 0, c2, -m, pk);
                         // the previous PV product is done: O is stable and the P columns are free
                         if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone, (gp - 1) & 1u, abort_flag, status))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        tmem_st32(trow + D64_P_COL, pk);
+                        rowsum += exp_half(x, 1, c2, -m, pk);
+                        tmem_st32(trow + D64_P_COL + 32, pk);
+                        slow = !__all_sync(0xffffffffu, rowsum <= 18446744073709551616.f);
                     }
-                    const bool rescale = (m_new != m) && j > 0;
-                    if (__any_sync(0xffffffffu, rescale)) {
-                        const float a = rescale ? alpha : 1.f;
+                    if (slow) {
+                        const float m_tile = row_max(x) * scale_log2;
+                        const float m_new = m_tile > m ? m_tile : m;
+                        alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
+                        const bool rescale = (m_new != m) && j > 0;
+                        if (__any_sync(0xffffffffu, rescale)) {
+                            const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            uint32_t o[32];
-                            tmem_ld32(trow + D64_O_COL + cc * 32, o);
-                            tmem_wait_ld();
+                            for (int cc = 0; cc < 2; ++cc) {
+                                uint32_t o[32];
+                                tmem_ld32(trow + D64_O_COL + cc * 32, o);
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                            tmem_st32(trow + D64_O_COL + cc * 32, o);
+                                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                                tmem_st32(trow + D64_O_COL + cc * 32, o);
+                            }
                         }
-                    }
-                    {
-                        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-                        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-                        tmem_st32(trow + D64_P_COL, p0);
-                        tmem_st32(trow + D64_P_COL + 32, p1);
+                        const float neg = m_new == -INFINITY ? 0.f : -m_new;
+                        uint32_t pk[32];
+                        rowsum = exp_half(x, 0, c2, neg, pk);
+                        tmem_st32(trow + D64_P_COL, pk);
+                        rowsum += exp_half(x, 1, c2, neg, pk);
+                        tmem_st32(trow + D64_P_COL + 32, pk);
+                        m = m_new;
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(bar_pfull);
                     ++gp;
                     l = l * alpha + rowsum;
-                    m = m_new;
                 }
                 // the gate pre-activations of this row, loaded while the last PV product runs
                 uint4 gv[GATE ? 8 : 1];

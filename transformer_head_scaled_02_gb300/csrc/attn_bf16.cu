@@ -84,57 +84,6 @@ static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 
 constexpr int A_THREADS = 384;
 
-
-
-__device__ __forceinline__ void drain_wait_a(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
-    }
-}
-
-// D(tmem) (+)= A(tmem) * B(smem): the A operand (M=128 rows, packed bf16 pairs along K)
-// comes from tensor memory.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-
-
 // One row of a 128-key score tile from TMEM into registers (warp-collective), with the
 // causal / key-length mask applied (keys [0, lim) are visible).
 __device__ __forceinline__ void load_s_tile(uint32_t taddr, bool masked, int kv0, int lim,
@@ -150,38 +99,6 @@ __device__ __forceinline__ void load_s_tile(uint32_t taddr, bool masked, int kv0
         for (int c = 0; c < 128; ++c)
             if (kv0 + c >= lim) x[c] = -INFINITY;
     }
-}
-
-// Row maximum of a score tile: 8 independent chains of 3-input max.
-__device__ __forceinline__ float row_max(const float (&x)[128]) {
-    float mk[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mk[k] = x[k];
-#pragma unroll
-    for (int c = 8; c < 128; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + k], x[c + 8 + k]);
-    return fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
-}
-
-// p = 2^(s*c + neg) for the 128 scores of a row; returns the row sum (fp32, 4 packed partial
-// sums) and writes P as packed bf16 pairs.
-__device__ __forceinline__ float exp_tile(const float (&x)[128], uint64_t c2, float neg,
-                                          uint32_t (&pk)[64]) {
-    const uint64_t neg2 = pack2(neg, neg);
-    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-    for (int k = 0; k < 64; ++k) {
-        float a0, a1;
-        unpack2(fma2(pack2(x[2 * k], x[2 * k + 1]), c2, neg2), a0, a1);
-        const float y0 = ex2_approx(a0), y1 = ex2_approx(a1);
-        acc[k & 3] = add2(acc[k & 3], pack2(y0, y1));
-        pk[k] = pack_bf16x2(y0, y1);
-    }
-    const uint64_t s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
-    float a0, a1;
-    unpack2(add2(s01, s23), a0, a1);
-    return a0 + a1;
 }
 
 // p = 2^(s*c + neg) for the 64 scores [64 h, 64 h + 64) of a row; returns their sum and

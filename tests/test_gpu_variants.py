@@ -207,3 +207,42 @@ def test_decode_long_cache_many_groups():
     B, Tmax = 2, 4133
     layer, got, ref = _decode_case(80, "bf16", B, Tq, Tmax, h, h_kv, d, [Tmax, 2049])
     assert_close(got, ref, "bf16", "decode MQA long")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("h_kv", [8, 2])
+def test_decode_ignores_cache_rows_past_the_length(d, h_kv):
+    """Cache rows at or past L_b are not part of the step (itwiki.kr "멀티 헤드 어텐션",
+    section 추론 비용과 변형: the cache holds the earlier tokens); they may hold anything, here
+    NaN, and the output must neither see them nor turn NaN (one row per cached head runs on
+    CUDA cores, grouped heads on the tensor core)."""
+    h, Tq = 8, 1
+    B, Tmax = 3, 700
+    lengths = [Tmax, 130, 513]
+    Q = wl.random_tensor((B, Tq, h * d), 85, "bf16")
+    Kc = wl.random_tensor((B, Tmax, h_kv * d), 86, "bf16")
+    Vc = wl.random_tensor((B, Tmax, h_kv * d), 87, "bf16")
+    Kn, Vn = Kc.copy(), Vc.copy()
+    for b, L in enumerate(lengths):
+        Kn[b, L:] = np.nan
+        Vn[b, L:] = np.nan
+    layer = Mha(h * d, h, d, d, dtype=torch.bfloat16, h_kv=h_kv)
+    lens = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    O = layer.decode(to_device(Q, "bf16"), to_device(Kn, "bf16"), to_device(Vn, "bf16"), lens)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    got = to_host(O)
+    assert np.isfinite(got).all()
+    assert_close(got, oracle.decode(Q, Kc, Vc, h, lengths, h_kv=h_kv), "bf16", "decode NaN tail")
+
+
+def test_decode_split_where_early_tokens_see_no_key():
+    """Several new tokens, MQA: with L = 258 the split that starts at key 256 holds no key
+    visible to new tokens 0 and 1 (they see keys up to 254 and 255); their records for that
+    split must carry no weight in the merge."""
+    h, h_kv, d, Tq = 16, 1, 64, 4
+    B, Tmax = 1, 1024
+    layer, got, ref = _decode_case(88, "bf16", B, Tq, Tmax, h, h_kv, d, [258])
+    assert layer.status() == 0
+    assert np.isfinite(got).all()
+    assert_close(got, ref, "bf16", "decode split without visible keys")

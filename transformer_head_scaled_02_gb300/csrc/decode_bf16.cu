@@ -578,18 +578,26 @@ __global__ void __launch_bounds__(DTC_THREADS, 1)
     }
 }
 
-// Keys per CTA for the tensor-core kernel: 128-key tiles, at least two per CTA, about two
-// CTAs per SM in total.
-int decode_span_tc(int B, int h_kv, int nrb, int T_max, int num_sms) {
+// Keys per CTA for the tensor-core kernel: the split count that minimises (waves of CTAs over
+// the resident slots) x (128-key tiles per CTA + a fixed cost of about three tiles for the
+// CTA's set-up: query gather, TMEM allocation, pipeline fill, partial record), splits at
+// least two tiles long.
+int decode_span_tc(int B, int h_kv, int nrb, int T_max, int num_sms, int ctas_per_sm) {
     const int64_t groups = (int64_t)B * h_kv * nrb;
-    const int64_t target = 2LL * (num_sms > 0 ? num_sms : 148);
-    int64_t splits = (target + groups - 1) / groups;
+    const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 148) * ctas_per_sm;
     const int64_t max_splits = (T_max + 2 * DTC_TK - 1) / (2 * DTC_TK);
-    if (splits > max_splits) splits = max_splits;
-    if (splits < 1) splits = 1;
-    int64_t span = (T_max + splits - 1) / splits;
-    span = (span + DTC_TK - 1) / DTC_TK * DTC_TK;
-    return (int)span;
+    int64_t best_span = 0, best_cost = -1;
+    for (int64_t s = 1; s <= max_splits; ++s) {
+        const int64_t span = ((T_max + s - 1) / s + DTC_TK - 1) / DTC_TK * DTC_TK;
+        const int64_t splits = (T_max + span - 1) / span;
+        const int64_t waves = (groups * splits + slots - 1) / slots;
+        const int64_t cost = waves * (span / DTC_TK + 3);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_span = span;
+        }
+    }
+    return (int)best_span;
 }
 
 // Keys per CTA: enough CTAs to fill the GPU a few times over, at least 4 tiles per CTA.
@@ -658,7 +666,7 @@ cudaError_t launch_decode_tc(const void* Q, int64_t ldq, const void* Kc, int64_t
         const uint64_t strides[2] = {(uint64_t)ldv * 2, (uint64_t)ldv * 2 * (uint64_t)T_max};
         if (!encode_tmap_bf16(&tV, Vc, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    const int span = decode_span_tc(B, h_kv, nrb, T_max, num_sms);
+    const int span = decode_span_tc(B, h_kv, nrb, T_max, num_sms, HD == 64 ? 2 : 1);
     const int n_splits = (T_max + span - 1) / span;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -463,7 +463,7 @@ def run_variant(args):
                 "config": {"variant": args.variant, "B": B, "T_q": Tq, "T_max": Tm, "h": h, "h_kv": hkv,
                            "d": d, "cache_lengths": "all T_max", "cache_bytes": cache,
                            "l2": "flushed before every timed step"},
-                "roofline": {"kernel": "decode (partial + merge)", "bound": "hbm", "achieved": round(gbs, 1),
+                "roofline": {"kernel": "decode_tc_kernel + decode_merge_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                              "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                              "peak_source": f"{pk_src} HBM copy"},
                 "gpu_launches": 2 * args.steps, "clocks": sampler.summary()}

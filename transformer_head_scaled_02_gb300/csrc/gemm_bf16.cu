@@ -48,6 +48,122 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Residual of one thread's row for the 64 columns of chunk c (zeros outside C).
+__device__ __forceinline__ void load_residual(const __nv_bfloat16* R, int64_t ldr, int row, int nc, int M,
+                                              int N, uint4 (&dst)[8]) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        dst[u] = row < M && nc + u * 8 < N
+                     ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)row * ldr + nc + u * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The bias of a tile's G_BN columns spread over one warp: lane l holds columns n0 + 8l .. 8l + 7
+// (N is a multiple of 8).  Loaded before the accumulator is ready, so that the epilogue reads
+// it by shuffles instead of waiting on global loads.
+__device__ __forceinline__ uint4 load_bias_lanes(const __nv_bfloat16* bias, int n0, int N, int lane) {
+    const int c = n0 + lane * 8;
+    return bias != nullptr && c < N ? __ldg(reinterpret_cast<const uint4*>(bias + c))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Keeps the compiler from moving reads of r above this point (the values written by a
+// tcgen05.ld are defined only after tcgen05.wait::ld).
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+        asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
+                     "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// Epilogue of one warp's share of an accumulator tile: 32 rows (the warp's TMEM lane quarter,
+// one row per thread, starting at row m0w of C) x G_BN columns from TMEM address t0, written as
+// C = acc + bias (+ R) in bf16 through the warp's two 4 KB staging buffers (buf0, buf0 + 4 KB)
+// and 32x64 TMA stores.  The TMEM read of chunk c + 1 is in flight while chunk c is converted,
+// so only the first read's latency is exposed; release() runs as soon as the whole accumulator
+// has been read, before the last chunk is converted.
+template <bool RESID, typename Release>
+__device__ __forceinline__ void epilogue_rows(uint32_t t0, uint4 bvec, bool has_bias, int m0w, int n0, int lane,
+                                              uint32_t buf0, uint32_t& bufsel, const CUtensorMap* tmC,
+                                              const __nv_bfloat16* R, int64_t ldr, int M, int N,
+                                              uint4 (&res)[RESID ? 8 : 1], Release release) {
+    constexpr int NCH = G_BN / 64;
+    uint32_t va[2][32], vb[2][32];
+    uint4 rnext[RESID ? 8 : 1];
+    const int row = m0w + lane;
+    tmem_ld32(t0, va[0]);
+    tmem_ld32(t0 + 32, va[1]);
+    tmem_wait_ld();
+    reg_fence(va[0]);
+    reg_fence(va[1]);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        uint32_t(&cur)[2][32] = (c & 1) ? vb : va;
+        uint32_t(&nxt)[2][32] = (c & 1) ? va : vb;
+        if (c + 1 < NCH) {
+            tmem_ld32(t0 + (c + 1) * 64, nxt[0]);
+            tmem_ld32(t0 + (c + 1) * 64 + 32, nxt[1]);
+        } else {
+            release();  // every column of the accumulator is in registers
+        }
+        if constexpr (RESID) {
+            if (c + 1 < NCH) load_residual(R, ldr, row, n0 + (c + 1) * 64, M, N, rnext);
+        }
+        const int nc = n0 + c * 64;
+        if (nc < N && m0w < M) {  // else the sub-tile lies wholly outside C
+            const uint32_t buf = buf0 + bufsel * (uint32_t)G_EPI_BUF;
+            if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
+            __syncwarp();
+            const uint32_t srow = buf + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(cur[u >> 2][(u & 3) * 8 + i]);
+                if constexpr (RESID) {
+                    const uint32_t rw[4] = {res[u].x, res[u].y, res[u].z, res[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[2 * i] += __uint_as_float(rw[i] << 16);
+                        x[2 * i + 1] += __uint_as_float(rw[i] & 0xFFFF0000u);
+                    }
+                }
+                if (has_bias) {
+                    const int src = c * 8 + u;
+                    const uint32_t bw[4] = {__shfl_sync(0xffffffffu, bvec.x, src),
+                                            __shfl_sync(0xffffffffu, bvec.y, src),
+                                            __shfl_sync(0xffffffffu, bvec.z, src),
+                                            __shfl_sync(0xffffffffu, bvec.w, src)};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[2 * i] += __uint_as_float(bw[i] << 16);
+                        x[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
+                    }
+                }
+                st_shared_v4(srow + ((uint32_t)(u ^ (lane & 7)) << 4), pack_bf16x2(x[0], x[1]),
+                             pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmC, buf, nc, m0w);
+                bulk_commit_group();
+            }
+            bufsel ^= 1u;
+        }
+        if constexpr (RESID) {
+            if (c + 1 < NCH)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) res[u] = rnext[u];
+        }
+        if (c + 1 < NCH) {
+            tmem_wait_ld();
+            reg_fence(nxt[0]);
+            reg_fence(nxt[1]);
+        }
+    }
+}
+
 // RESID: the epilogue adds the residual R (a separate instantiation, so that the plain
 // projection carries none of its code or registers).
 template <bool RESID>
@@ -203,80 +319,21 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const int n0 = (tile / num_m) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            // the residual of this thread's row: the first 64 columns are loaded while the
-            // tile's MMAs run, each next 64 while the current ones are written out
-            const int rrow = m0 + q * 32 + lane;
-            auto load_res = [&](int c, uint4 (&dst)[8]) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[u] = rrow < M && n0 + c * 64 + u * 8 < N
-                                 ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)rrow * ldr + n0 + c * 64 + u * 8))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            };
-            uint4 rcur[RESID ? 8 : 1], rnext[RESID ? 8 : 1];
-            if constexpr (RESID) load_res(0, rcur);
+            // bias and the first 64 residual columns are fetched while the tile's MMAs run
+            const uint4 bvec = load_bias_lanes(bias, n0, N, lane);
+            uint4 res[RESID ? 8 : 1];
+            if constexpr (RESID) load_residual(R, ldr, m0 + q * 32 + lane, n0, M, N, res);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
                 break;
             tc_fence_after();
-            const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
-#pragma unroll 1
-            for (int c = 0; c < G_BN / 64; ++c) {
-                if constexpr (RESID) {
-                    if (c > 0)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) rcur[u] = rnext[u];
-                    if (c + 1 < G_BN / 64) load_res(c + 1, rnext);
-                }
-                uint32_t v[2][32];
-                tmem_ld32(t0 + c * 64, v[0]);
-                tmem_ld32(t0 + c * 64 + 32, v[1]);
-                tmem_wait_ld();
-                if (c == G_BN / 64 - 1) {
-                    // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    mbar_arrive(bar_tempty + 8u * acc);
-                }
-                const int nc = n0 + c * 64;
-                if (nc >= N || m0 + q * 32 >= M) continue;  // sub-tile wholly outside C
-                const uint32_t buf = sE + (uint32_t)((e * 2 + (int)bufsel) * G_EPI_BUF);
-                if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
-                __syncwarp();
-                const uint32_t row = buf + (uint32_t)lane * 128u;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float x[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
-                    if constexpr (RESID) {
-                        const uint32_t rw[4] = {rcur[u].x, rcur[u].y, rcur[u].z, rcur[u].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            x[2 * i] += __uint_as_float(rw[i] << 16);
-                            x[2 * i + 1] += __uint_as_float(rw[i] & 0xFFFF0000u);
-                        }
-                    }
-                    if (bias != nullptr && nc + u * 8 < N) {
-                        const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
-                        const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            x[2 * i] += __uint_as_float(bw[i] << 16);
-                            x[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
-                        }
-                    }
-                    st_shared_v4(row + ((uint32_t)(u ^ (lane & 7)) << 4), pack_bf16x2(x[0], x[1]),
-                                 pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                                 pack_bf16x2(x[6], x[7]));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmC, buf, nc, m0 + q * 32);
-                    bulk_commit_group();
-                }
-                bufsel ^= 1u;
-            }
+            epilogue_rows<RESID>(tmem_base + lane_off + (uint32_t)(acc * G_BN), bvec, bias != nullptr,
+                                 m0 + q * 32, n0, lane, sE + (uint32_t)(e * 2 * G_EPI_BUF), bufsel, &tmC, R,
+                                 ldr, M, N, res, [&] {
+                                     // accumulator read: hand it back to the MMA warp
+                                     tc_fence_before();
+                                     mbar_arrive(bar_tempty + 8u * acc);
+                                 });
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -476,86 +533,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             const int n0 = (tile / num_m) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            // the residual of this thread's row: the first 64 columns are loaded while the
-            // tile's MMAs run, each next 64 while the current ones are written out
-            const int rrow = m0 + q * 32 + lane;
-            auto load_res = [&](int c, uint4 (&dst)[8]) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[u] = rrow < M && n0 + c * 64 + u * 8 < N
-                                 ? __ldg(reinterpret_cast<const uint4*>(R + (int64_t)rrow * ldr + n0 + c * 64 + u * 8))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            };
-            uint4 rcur[RESID ? 8 : 1], rnext[RESID ? 8 : 1];
-            if constexpr (RESID) load_res(0, rcur);
+            // bias and the first 64 residual columns are fetched while the tile's MMAs run
+            const uint4 bvec = load_bias_lanes(bias, n0, N, lane);
+            uint4 res[RESID ? 8 : 1];
+            if constexpr (RESID) load_residual(R, ldr, m0 + q * 32 + lane, n0, M, N, res);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
                 break;
             tc_fence_after();
-            const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * G_BN);
-#pragma unroll 1
-            for (int c = 0; c < G_BN / 64; ++c) {
-                if constexpr (RESID) {
-                    if (c > 0)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) rcur[u] = rnext[u];
-                    if (c + 1 < G_BN / 64) load_res(c + 1, rnext);
-                }
-                uint32_t v[2][32];
-                tmem_ld32(t0 + c * 64, v[0]);
-                tmem_ld32(t0 + c * 64 + 32, v[1]);
-                tmem_wait_ld();
-                if (c == G_BN / 64 - 1) {
-                    // accumulator fully read: release it to the MMA issuer in the even CTA
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (leader)
-                            mbar_arrive(bar_tempty + 8u * acc);
-                        else
-                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * acc, 0));
-                    }
-                }
-                const int nc = n0 + c * 64;
-                if (nc >= N || m0 + q * 32 >= M) continue;  // sub-tile wholly outside C
-                const uint32_t buf = sE + (uint32_t)((e * 2 + (int)bufsel) * G_EPI_BUF);
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t row = buf + (uint32_t)lane * 128u;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float x[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(v[u >> 2][(u & 3) * 8 + i]);
-                    if constexpr (RESID) {
-                        const uint32_t rw[4] = {rcur[u].x, rcur[u].y, rcur[u].z, rcur[u].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            x[2 * i] += __uint_as_float(rw[i] << 16);
-                            x[2 * i + 1] += __uint_as_float(rw[i] & 0xFFFF0000u);
-                        }
-                    }
-                    if (bias != nullptr && nc + u * 8 < N) {
-                        const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + nc + u * 8));
-                        const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            x[2 * i] += __uint_as_float(bw[i] << 16);
-                            x[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
-                        }
-                    }
-                    st_shared_v4(row + ((uint32_t)(u ^ (lane & 7)) << 4), pack_bf16x2(x[0], x[1]),
-                                 pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                                 pack_bf16x2(x[6], x[7]));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmC, buf, nc, m0 + q * 32);
-                    bulk_commit_group();
-                }
-                bufsel ^= 1u;
-            }
+            epilogue_rows<RESID>(tmem_base + lane_off + (uint32_t)(acc * G_BN), bvec, bias != nullptr,
+                                 m0 + q * 32, n0, lane, sE + (uint32_t)(e * 2 * G_EPI_BUF), bufsel, &tmC, R,
+                                 ldr, M, N, res, [&] {
+                                     // accumulator read: release it to the MMA issuer in the even CTA
+                                     tc_fence_before();
+                                     __syncwarp();
+                                     if (lane == 0) {
+                                         if (leader)
+                                             mbar_arrive(bar_tempty + 8u * acc);
+                                         else
+                                             mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * acc, 0));
+                                     }
+                                 });
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

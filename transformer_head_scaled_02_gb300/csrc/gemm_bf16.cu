@@ -67,15 +67,6 @@ __device__ __forceinline__ uint4 load_bias_lanes(const __nv_bfloat16* bias, int 
                                     : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Keeps the compiler from moving reads of r above this point (the values written by a
-// tcgen05.ld are defined only after tcgen05.wait::ld).
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 8)
-        asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
-                     "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
-}
-
 // Epilogue of one warp's share of an accumulator tile: 32 rows (the warp's TMEM lane quarter,
 // one row per thread, starting at row m0w of C) x G_BN columns from TMEM address t0, written as
 // C = acc + bias (+ R) in bf16 through the warp's two 4 KB staging buffers (buf0, buf0 + 4 KB)

@@ -64,6 +64,8 @@ def _oracle_forward(w, x, rows=None):
     (1, 64, 64, True),          # one row
     (300, 1024, 3072, True),    # ragged M, several N tiles
     (257, 72, 200, False),      # K tail inside a 64-wide block, N tail inside a 256-wide tile
+    (300, 64, 256, True),       # one 64-wide K half: the second half of the stage is skipped
+    (260, 192, 520, False),     # K = 1.5 stages of 128
     (1024, 512, 1536, True),
 ])
 def test_linear_step(dtype, M, K, N, bias):

@@ -355,11 +355,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 //                        MMA issuer; its commits are multicast to both CTAs' barriers;
 //   warps 2..5 (both)    epilogue of the CTA's own 128 rows, as above; they release the
 //                        accumulator by arriving on the even CTA's barrier.
-constexpr int P_BK = 64;
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = 128 * P_BK * 2;          // 16 KB: this CTA's 128 rows of A
-constexpr int P_B_CHUNK = P_BK * 64 * 2;           // 8 KB: 64 K-rows x 64 N-columns
-constexpr int P_B_BYTES = P_BK * 128 * 2;          // 16 KB: this CTA's half of B
+// Tiles are numbered with N fastest, so the pairs running at the same time work on the same
+// 256 rows of A (read from HBM once, then from L2) while the weights, a few MB, stay in L2;
+// numbered M-first, every column block re-read the whole of A (a 65536 x 768 A six times).
+// A stage holds 128 K-columns as two 64-wide halves (the 128-byte swizzle atom is 64 bf16
+// wide): per CTA and half, one 128-row A box and two 64x64 B boxes.  A half that lies wholly
+// past K is neither loaded nor multiplied.
+constexpr int P_BK = 128;
+constexpr int P_STAGES = 3;
+constexpr int P_HALF_A = 128 * 64 * 2;             // 16 KB: 128 rows x 64 K of A
+constexpr int P_B_CHUNK = 64 * 64 * 2;             // 8 KB: 64 K-rows x 64 N-columns
+constexpr int P_HALF_B = 2 * P_B_CHUNK;            // 16 KB: 64 K-rows x this CTA's 128 columns
+constexpr int P_A_BYTES = 2 * P_HALF_A;            // 32 KB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = 2 * P_HALF_B;            // 32 KB: this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + 1024;
 
@@ -437,20 +445,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                const int m0 = (tile % num_m) * 256 + (int)rank * 128;
-                const int nb = (tile / num_m) * G_BN + (int)rank * 128;
+                const int m0 = (tile / num_n) * 256 + (int)rank * 128;
+                const int nb = (tile % num_n) * G_BN + (int)rank * 128;
                 for (int kb = 0; kb < num_k; ++kb) {
                     if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = mapa_shared(bar_full + 8u * stage, 0);
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8u * stage, 2 * P_STAGE_BYTES);
-                    tma_load_2d_pair(sA + stage * P_A_BYTES, &tmA, kb * P_BK, m0, fb);
+                    const int halves = kb * P_BK + 64 < K ? 2 : 1;
+                    if (leader)
+                        mbar_arrive_expect_tx(bar_full + 8u * stage, 2 * halves * (P_HALF_A + P_HALF_B));
+                    for (int hh = 0; hh < halves; ++hh) {
+                        const int k0 = kb * P_BK + hh * 64;
+                        tma_load_2d_pair(sA + stage * P_A_BYTES + hh * P_HALF_A, &tmA, k0, m0, fb);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_2d_pair(sB + stage * P_B_BYTES + c * P_B_CHUNK, &tmW, nb + c * 64,
-                                         kb * P_BK, fb);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d_pair(sB + stage * P_B_BYTES + hh * P_HALF_B + c * P_B_CHUNK, &tmW,
+                                             nb + c * 64, k0, fb);
+                    }
                     ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -494,10 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                     tc_fence_after();
                     const uint64_t ad = adesc0 + (uint64_t)((stage * P_A_BYTES) >> 4);
                     const uint64_t bd = bdesc0 + (uint64_t)((stage * P_B_BYTES) >> 4);
-#pragma unroll
-                    for (int k = 0; k < P_BK / 16; ++k)
-                        mma_bf16_ss_pair(d_tmem, ad + (uint64_t)((k * 32) >> 4),
-                                         bd + (uint64_t)((k * 2048) >> 4), idesc,
+                    const int ksteps = kb * P_BK + 64 < K ? P_BK / 16 : 64 / 16;
+                    for (int k = 0; k < ksteps; ++k)
+                        mma_bf16_ss_pair(d_tmem, ad + (uint64_t)(((k >> 2) * P_HALF_A + (k & 3) * 32) >> 4),
+                                         bd + (uint64_t)(((k >> 2) * P_HALF_B + (k & 3) * 2048) >> 4), idesc,
                                          (kb | k) != 0 ? 1u : 0u);
                     tc_commit_pair_mc(bar_empty + 8u * stage, 0x3);
                     if (++stage == P_STAGES) {
@@ -520,8 +533,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         uint32_t bufsel = 0;
         int it = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
-            const int m0 = (tile % num_m) * 256 + (int)rank * 128;
-            const int n0 = (tile / num_m) * G_BN;
+            const int m0 = (tile / num_n) * 256 + (int)rank * 128;
+            const int n0 = (tile % num_n) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // bias and the first 64 residual columns are fetched while the tile's MMAs run

@@ -7,37 +7,33 @@
 // iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", sections 9-10 (mask as -inf,
 // row softmax) and 19 (cross-attention).
 //
-// One CTA computes two 128-row query tiles (Q0, Q1: 256 consecutive rows) of one
-// (batch, head); both tiles share every K/V tile the TMA brings in, which halves the
-// L2->SMEM traffic per FLOP.  The softmax is the online form: a running row maximum m and
-// sum l, with O rescaled when m grows, so the result equals the row softmax after the final
-// division by l.  Everything stays in base 2: p = 2^(s*c - m) with c = log2(e)/sqrt(d) folded
-// into one FMA per score.
+// Two kernels share the softmax scheme below:
+//   attn_bf16_tc_kernel   d = 128: one CTA = two 128-row query tiles of one (batch, head)
+//                         that share every K/V tile the TMA brings in;
+//   attn_bf16_d64_kernel  d = 64: persistent, two CTAs per SM, one query tile at a time
+//                         (described with the kernel further down).
+// The softmax is the online form: a running row maximum m and sum l, with O rescaled when m
+// grows, so the result equals the row softmax after the final division by l.  Everything
+// stays in base 2: p = 2^(s*c - m) with c = log2(e)/sqrt(d) folded into one FMA per score.
 //
-// Tensor memory (512 columns, one CTA per SM):
-//   S_t  [128 t, 128 t + 128)        scores of query tile t, fp32
-//   O_t  [256 + d t, 256 + d t + d)  output accumulator of tile t, fp32
-//   P_t  d = 64:  [384 + 64 t, +64)  probabilities as packed bf16 pairs, own columns
-//        d = 128: the first 64 columns of S_t (TMEM is full: S0, S1, O0, O1 use all 512)
+// d = 128 tensor memory (512 columns, one CTA per SM):
+//   S_t  [128 t, 128 t + 128)          scores of query tile t, fp32
+//   O_t  [256 + 128 t, 256 + 128 t + 128)  output accumulator of tile t, fp32
+//   P_t  the first 64 columns of S_t (TMEM is full: S0, S1, O0, O1 use all 512)
 // The PV product reads P from TMEM (A operand in tensor memory); Q and K come from shared
-// memory.  With its own P columns (d = 64) the scores of key tile j+1 are computed while
-// the softmax of tile j is still running; with P inside S (d = 128) S_{j+1} must wait
-// until P_j has been consumed, and the two query tiles take turns on the tensor core.
+// memory.  With P inside S, S_{j+1} must wait until P_j has been consumed, and the two
+// query tiles take turns on the tensor core.
 //
-// Warp roles (384 threads):
+// d = 128 warp roles (384 threads):
 //   warp 0      TMA: Q0 and Q1 once, then K and V tiles (128 keys) into a ring of stages;
-//   warp 1      TMEM owner and MMA issuer.  Per key tile j:
-//                 d = 64:  warp 1 issues the score MMAs S_t(j+1) (as soon as the softmax
-//                          has read S_t(j)), warp 2 the PV MMAs O_t += P_t V_j (as soon as P_t
-//                          is in TMEM), for both query tiles;
-//                 d = 128: warp 1 alone, alternating the tiles:
-//                          O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j, S_1(j+1)
+//   warp 1      TMEM owner and MMA issuer, alternating the tiles per key tile j:
+//                 O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j, S_1(j+1)
 //               (tcgen05 MMAs of one thread execute in issue order, so S_t may overwrite the
 //               P_t columns right after the MMA that reads them);
 //   warps 2-3   otherwise idle;
 //   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1 -- one row per thread (TMEM
-//               lane = row): read S, mask, row max, exponentials, row sum, P -> TMEM, lazy
-//               O rescale; while one group works, the tensor core runs the other tile's MMAs.
+//               lane = row): read S, mask, exponentials, row sum, P -> TMEM, lazy O rescale;
+//               while one group works, the tensor core runs the other tile's MMAs.
 //               At the end O/l is rounded to bf16 and stored by TMA straight into column
 //               block (head * d) of the (B, T, h*d) Concat output.
 // Reference maximum: P = 2^(s*c - m_ref) gives the same O / l for any reference m_ref (the
@@ -63,23 +59,15 @@ struct AttnCfg {
     static constexpr int CHUNK = 128 * 128;         // 128 rows x 64 bf16 (128 B) = 16 KB
     static constexpr int Q_BYTES = CH * CHUNK;      // one query tile
     static constexpr int KV_BYTES = CH * CHUNK;     // one K (or V) tile
-    static constexpr int STAGES = HD == 64 ? 5 : 2;
+    static constexpr int STAGES = 2;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = NQ * Q_BYTES + 2 * STAGES * KV_BYTES + BAR_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr bool SEP_P = HD == 64;  // P in its own TMEM columns
-    // MMA-issuing threads: with P in its own columns, one for the score MMAs and one for the
-    // PV MMAs (independent chains); with P inside S, one for everything, strictly alternating
-    // the tiles, which keeps the two softmax groups out of phase.
-    static constexpr int ISSUERS = SEP_P ? 2 : 1;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return (uint32_t)(128 * t); }
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return (uint32_t)(256 + HD * t); }
-    __host__ __device__ static constexpr uint32_t P_COL(int t) {
-        return SEP_P ? (uint32_t)(384 + 64 * t) : (uint32_t)(128 * t);
-    }
+    __host__ __device__ static constexpr uint32_t P_COL(int t) { return (uint32_t)(128 * t); }
 };
 
-static_assert(AttnCfg<64>::SMEM <= 232448, "smem budget d=64");
 static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 
 constexpr int A_THREADS = 384;
@@ -142,6 +130,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         int causal, const int32_t* __restrict__ kv_lengths,
                         const __nv_bfloat16* __restrict__ gate, int64_t ldg, float scale_log2,
                         int* status) {
+    static_assert(HD == 128, "head dim 64 runs on attn_bf16_d64_kernel");
     using C = AttnCfg<HD>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -189,7 +178,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             mbar_init(bar_pfull + 8u * t, 128);
             mbar_init(bar_pvdone + 8u * t, 1);
         }
-        mbar_init(bar_drain, C::ISSUERS);
+        mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -260,74 +249,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 drain_wait_a(bar_vfull + 8u * st, ph);
             }
         }
-    } else if (C::ISSUERS == 2 && (warp == 1 || warp == 2)) {
-        if (lane == 0) {
-            // ---------------- MMA issuers for d = 64: warp 1 issues every score MMA, warp 2
-            // every PV MMA, both query tiles.  tcgen05.mma issue is paced by the tensor core
-            // (the issuing thread stalls while its queue is full), so one thread's waits would
-            // idle the tensor core; and with P in its own TMEM columns the two chains are
-            // independent: S_t(j+1) needs only the softmax's read of S_t(j), PV_t(j) only P_t(j).
-            // Per query tile the MMAs still execute in issue order within each chain.
-            const uint32_t idesc_s = idesc_bf16_f32(128, C::BN, false, false);
-            const uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
-            const uint64_t kdesc0 = sdesc_sw128(sK, 16, 1024);
-            const uint64_t vdesc0 = sdesc_sw128(sV, C::CHUNK, 1024);
-            const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
-            bool ok = true;
-            if (warp == 1) {
-                // scores: S_t(j) = Q_t K_j^T, signalled on s_full_t
-                auto issue_s = [&](int t, int j) {
-                    const uint64_t kdesc = kdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
-                    const uint64_t qdesc = qdesc0 + (uint64_t)((t * C::Q_BYTES) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off16 = (uint32_t)(((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4);
-                        mma_bf16_ss(tmem_base + C::S_COL(t), qdesc + off16, kdesc + off16, idesc_s,
-                                    kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar_sfull + 8u * t);
-                };
-                for (int j = 0; j < n_max && ok; ++j) {
-                    ok = (j == 0 ? mbar_wait(bar_q, 0, abort_flag, status) : true) &&
-                         mbar_wait(bar_kfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
-#pragma unroll
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j >= n_t[t]) continue;
-                        // S_t(j) may overwrite S_t only once the softmax has read S_t(j-1)
-                        if (j > 0)
-                            ok = mbar_wait(bar_sfree + 8u * t, (uint32_t)(j - 1) & 1u, abort_flag, status);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_s(t, j);
-                    }
-                }
-            } else {
-                // weighted sums: O_t += P_t V_j, signalled on pv_done_t; then the stage of key
-                // tile j is released (the score MMAs that read K_j completed before P_t(j) could
-                // be written)
-                for (int j = 0; j < n_max && ok; ++j) {
-                    ok = mbar_wait(bar_vfull + 8u * (j % S), (uint32_t)(j / S) & 1u, abort_flag, status);
-                    const uint64_t vdesc = vdesc0 + (uint64_t)(((j % S) * C::KV_BYTES) >> 4);
-#pragma unroll
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (j >= n_t[t]) continue;
-                        ok = mbar_wait(bar_pfull + 8u * t, (uint32_t)j & 1u, abort_flag, status);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < C::BN / 16; ++kk)
-                            mma_bf16_ts(tmem_base + C::O_COL(t), tmem_base + C::P_COL(t) + kk * 8,
-                                        vdesc + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                        (j > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bar_pvdone + 8u * t);
-                    }
-                    if (ok) tc_commit(bar_kvempty + 8u * (j % S));
-                }
-            }
-            tc_commit(bar_drain);
-            drain_wait_a(bar_drain, 0);
-        }
-    } else if (C::ISSUERS == 1 && warp == 1) {
+    } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- single MMA issuer for both query tiles, strictly alternating:
             //   O_0 += P_0 V_j ; S_0(j+1) ; O_1 += P_1 V_j ; S_1(j+1)
@@ -437,19 +359,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 uint32_t pk[64];
                 float x[128];
                 float rowsum, alpha = 1.f, m_new = m;
-                if constexpr (C::SEP_P) {
-                    // P has its own columns: S_t(j) is released right after it is read, so the
-                    // scores of the next key tile are computed while this softmax runs.  The
-                    // tile maximum is always computed; the reference moves only when it would
-                    // otherwise let P exceed 2^32.
-                    load_s_tile(trow + C::S_COL(t), masked, kv0, lim, x);
-                    tc_fence_before();
-                    mbar_arrive(bar_sfree + 8u * t);
-                    const float m_tile = row_max(x) * scale_log2;
-                    if (m_tile > m + 32.0f) m_new = m_tile;
-                    alpha = ex2_approx(m - m_new);  // 0 on the first tile (m = -inf)
-                    rowsum = exp_tile(x, pack2(scale_log2, scale_log2), m_new == -INFINITY ? 0.f : -m_new, pk);
-                } else {
+                {
                     // P overwrites S in place, so S_t(j) stays readable until P is written.
                     // Fast path (every key tile after the first): no row maximum.  P is computed
                     // against the current reference m; any reference gives the same O / l, it
@@ -472,16 +382,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     }
                 }
                 const bool rescale = (m_new != m) && j > 0;
-                if (C::SEP_P && j > 0) {
-                    // PV_t(j-1) done: O_t is stable and the P_t columns are free
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_pvdone + 8u * t, (uint32_t)(j - 1) & 1u,
-                                                           abort_flag, status))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                // (P inside S: S_t(j) was issued after PV_t(j-1), so O_t is already complete)
+                // S_t(j) was issued after PV_t(j-1), so O_t is already complete
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float a = rescale ? alpha : 1.f;
 #pragma unroll
@@ -594,7 +495,9 @@ constexpr int D64_THREADS = 256;
 constexpr int D64_REGS_CTRL = 56;
 constexpr int D64_REGS_SOFTMAX = 200;
 constexpr int D64_TILE = 128 * 128;  // one 128-row x 64-column bf16 box, 16 KB
-constexpr int D64_BAR_BYTES = 256;
+constexpr int D64_BAR_BYTES = 512;
+// batches ordered by key length (longest first) when the lengths vary: up to this many
+constexpr int D64_SORT_MAX_B = 64;
 constexpr int D64_SMEM = D64_TILE * (2 + DK_STAGES + DV_STAGES) + D64_BAR_BYTES + 1024;
 // two CTAs (each with its 1 KB of reserved shared memory) must fit one SM's 228 KB
 static_assert(2 * (D64_SMEM + 1024) <= 233472, "two d=64 CTAs per SM");
@@ -608,15 +511,28 @@ struct D64Item {
     bool bad;
 };
 
-// Item k of the longest-first numbering.
+// Item k of the longest-first numbering.  Causal: by query tile, the last tiles of every
+// (batch, head) first.  With key lengths and no causal mask (bperm: the batches sorted by
+// length, longest first): by batch in that order, then head, then query tile, so that the
+// items dealt out at one time share their K/V tiles.
 __device__ __forceinline__ D64Item d64_item(int k, int BH, int h, int group, int n_qt, int causal,
-                                            const int32_t* kv_lengths, int T_kv) {
+                                            const int32_t* kv_lengths, int T_kv, const int* bperm) {
     D64Item it;
-    const int rank = k / BH;
-    const int bh = k - rank * BH;
-    const int qt = causal ? n_qt - 1 - rank : rank;
-    it.b = bh / h;
-    it.head = bh - it.b * h;
+    int qt;
+    if (bperm != nullptr) {
+        const int per_b = h * n_qt;
+        const int bs = k / per_b;
+        const int rem = k - bs * per_b;
+        it.b = bperm[bs];
+        it.head = rem / n_qt;
+        qt = rem - it.head * n_qt;
+    } else {
+        const int rank = k / BH;
+        const int bh = k - rank * BH;
+        qt = causal ? n_qt - 1 - rank : rank;
+        it.b = bh / h;
+        it.head = bh - it.b * h;
+    }
     it.kvh = it.head / group;
     it.qrow0 = qt * 128;
     const int L = kv_lengths != nullptr ? kv_lengths[it.b] : T_kv;
@@ -632,7 +548,9 @@ __device__ __forceinline__ int d64_item_index(int r, int G, int c) {
     return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
-template <bool GATE>
+// SORTED: key lengths given, no causal mask, B <= D64_SORT_MAX_B -- items by batch, longest
+// first (a separate instantiation: the plain order's code is left exactly as it is)
+template <bool GATE, bool SORTED>
 __global__ void __launch_bounds__(D64_THREADS, 2)
     attn_bf16_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -666,6 +584,7 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
     const uint32_t bar_drain = bar_pvdone + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* bperm_s = reinterpret_cast<int*>(gbase + (bar_drain + 16u - base));  // [D64_SORT_MAX_B]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -674,10 +593,11 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
     const int N = BH * n_qt;
     const int G = (int)gridDim.x;
     const int c = (int)blockIdx.x;
+    const int* bperm = SORTED ? bperm_s : nullptr;
     int R = 0;  // items of this CTA
     while (d64_item_index(R, G, c) < N) ++R;
     auto item = [&](int r) {
-        return d64_item(d64_item_index(r, G, c), BH, h, h / h_kv, n_qt, causal, kv_lengths, T_kv);
+        return d64_item(d64_item_index(r, G, c), BH, h, h / h_kv, n_qt, causal, kv_lengths, T_kv, bperm);
     };
 
     if (threadIdx.x == 0) {
@@ -713,6 +633,20 @@ __global__ void __launch_bounds__(D64_THREADS, 2)
     // Q, K, V and the key lengths may come from the previous kernel on the stream
     grid_dependency_wait();
     grid_launch_dependents();
+    if constexpr (SORTED) {
+        // rank of each batch by key length (longest first, ties by index)
+        if (threadIdx.x < B) {
+            const int t = (int)threadIdx.x;
+            const int Lt = kv_lengths[t];
+            int rank = 0;
+            for (int u = 0; u < B; ++u) {
+                const int Lu = kv_lengths[u];
+                rank += (Lu > Lt) || (Lu == Lt && u < t);
+            }
+            bperm_s[rank] = t;
+        }
+        __syncthreads();
+    }
 
     if (warp < 4) {
       setmaxnreg_dec<D64_REGS_CTRL>();
@@ -1034,17 +968,18 @@ cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t l
     }
     // setmaxnreg.inc waits until the CTA's register pool (threads x registers at launch) can
     // grant the rise: refuse to launch a build whose register count cannot cover the split
-    static int pool_ok[2] = {-1, -1};
-    int& ok = pool_ok[G != nullptr];
+    const bool sorted = kv_lengths != nullptr && !causal && B <= D64_SORT_MAX_B;
+    auto kernel = G != nullptr ? (sorted ? attn_bf16_d64_kernel<true, true> : attn_bf16_d64_kernel<true, false>)
+                               : (sorted ? attn_bf16_d64_kernel<false, true> : attn_bf16_d64_kernel<false, false>);
+    static int pool_ok[4] = {-1, -1, -1, -1};
+    int& ok = pool_ok[(G != nullptr ? 2 : 0) + (sorted ? 1 : 0)];
     if (ok < 0) {
         cudaFuncAttributes fa;
-        const cudaError_t e = cudaFuncGetAttributes(
-            &fa, G != nullptr ? attn_bf16_d64_kernel<true> : attn_bf16_d64_kernel<false>);
+        const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
         ok = fa.numRegs * D64_THREADS >= 128 * (D64_REGS_CTRL + D64_REGS_SOFTMAX) ? 1 : 0;
     }
     if (!ok) return cudaErrorInvalidConfiguration;
-    auto kernel = G != nullptr ? attn_bf16_d64_kernel<true> : attn_bf16_d64_kernel<false>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D64_SMEM);
     if (err != cudaSuccess) return err;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt(64.0));
@@ -1103,18 +1038,11 @@ cudaError_t launch_attn_bf16(const void* Q, int64_t ldq, const void* K, int64_t 
                              int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d, int causal,
                              const int32_t* kv_lengths, int num_sms, int* status,
                              cudaStream_t stream) {
-    // d = 64: causal self-attention without key lengths (query tiles of a head differ only in
-    // their causal length, and the lengths are known here) runs on the persistent kernel,
-    // whose fixed item order balances them; with key lengths (known only on the device) or
-    // without the causal mask, every item is long and the CTA-per-tile-pair kernel, whose
-    // two query tiles share each K/V tile and whose CTAs the hardware schedules as they
-    // finish, is the better fit
-    if (d == 64 && causal && kv_lengths == nullptr)
+    // d = 64: the persistent kernel, two CTAs per SM, whose fixed longest-first item order
+    // balances the causal triangle and, with key lengths, the batches' lengths
+    if (d == 64)
         return launch_attn_d64(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
                                kv_lengths, num_sms, status, stream);
-    if (d == 64)
-        return launch_attn_hd<64>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
-                                  kv_lengths, status, stream);
     if (d == 128)
         return launch_attn_hd<128>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, T_kv, causal,
                                    kv_lengths, status, stream);

@@ -285,7 +285,10 @@ def run_ours(args):
         raise RuntimeError("device status reports an error after the timed region")
 
     fl = wl.flops(w, x["kv_lengths"])
-    step_flops = fl["total"]
+    # with key padding, only the valid keys count: the padded ones need neither projection nor
+    # attention, and the kernels skip them (the nominal count is reported beside it)
+    step_flops = fl.get("alg_total", fl["total"])
+    flops_counted = "algorithmic (valid keys only)" if "alg_total" in fl else "nominal"
     value = world * step_flops / (ms_per_step / 1e3) / 1e12
 
     # ---------------- per-kernel durations: the same three launches, events between them
@@ -330,7 +333,10 @@ def run_ours(args):
             e[0].record()
             layer.linear(Xq2, Wqkv[:, :hq], bq, out=qb.view(-1, hq))
             e[1].record()
-            layer.linear(Xkv2, Wqkv[:, hq:], bkv, out=kvb.view(-1, hk + hv))
+            if kvl is None:
+                layer.linear(Xkv2, Wqkv[:, hq:], bkv, out=kvb.view(-1, hk + hv))
+            else:  # as the forward runs it: rows past the key lengths are not projected
+                layer.linear_segments(Xkv2, Wqkv[:, hq:], bkv, kvl, w.T_kv, out=kvb.view(-1, hk + hv))
             e[2].record()
             layer.attention(qb, kvb[..., :hk], kvb[..., hk:], causal=w.causal, kv_lengths=kvl,
                             out=ocat)
@@ -344,9 +350,10 @@ def run_ours(args):
                       "attention": launch_ms["attention"], "out_proj": launch_ms["out_proj"]}
         if x["kv_lengths"] is not None:
             import numpy as np
-            # the attention kernel visits only the L_b valid keys of each batch
+            # the kernels visit only the L_b valid keys of each batch
             L = float(np.sum(np.asarray(x["kv_lengths"], dtype=np.float64)))
-            sf = dict(sf, attention=2.0 * w.h * w.T_q * L * (w.d_k + w.d_v) * (0.5 if w.causal else 1.0))
+            sf = dict(sf, attention=2.0 * w.h * w.T_q * L * (w.d_k + w.d_v) * (0.5 if w.causal else 1.0),
+                      qkv_proj=2.0 * w.D * (w.B * w.T_q * hq + L * (hk + hv)))
 
     # ---------------- end to end through the public API, host buffers in and out
     xh = d["X_q"].cpu().pin_memory()
@@ -402,7 +409,9 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights; no dataset)",
         "config": {"workload": w.name, "B": w.B, "T_q": w.T_q, "T_kv": w.T_kv, "D": w.D,
                    "h": w.h, "d_k": w.d_k, "d_v": w.d_v, "causal": w.causal, "cross": w.cross,
-                   "flops_per_step": step_flops, "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
+                   "flops_per_step": step_flops, "flops_counted": flops_counted,
+                   "nominal_flops_per_step": fl["total"],
+                   "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
                    "peak_tflops": pk["bf16_tflops"], "peak_source": pk_src,
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

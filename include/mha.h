@@ -220,6 +220,25 @@ mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K,
                          int64_t ldr, void* C, int64_t ldc, void* stream);
 
 /*
+ * mha_linear_segments -- mha_linear for the key/value projection of cross-attention with key
+ * padding (molayo1419.me "MHA란 무엇인가?", pitfalls 2 and 3: padded keys are excluded, so
+ * their projections are never used).  The M rows form M / seg_rows segments of seg_rows
+ * consecutive rows (segment b = batch b of a (B, T_kv, *) tensor, seg_rows = T_kv);
+ * seg_len is a device int32[M / seg_rows] of valid lengths.  Rows of segment b at or past
+ * seg_len[b] rounded up to a multiple of 128 may be left unwritten (their contents are then
+ * unspecified); every other row is exactly what mha_linear writes.  The attention step
+ * (mha_attention with the same lengths) reads only whole 128-key tiles up to each length, so
+ * it never reads an unwritten row.  The skipped rows are whole 256-row blocks; for fp32
+ * handles, or more than 131072 rows, every row is written.
+ * seg_len NULL, seg_rows <= 0 or M not a multiple of seg_rows: MHA_ERR_INVALID_ARG; other
+ * arguments as for mha_linear.
+ */
+mha_status mha_linear_segments(mha_t handle, const void* A, int64_t lda, int M, int K,
+                               const void* W, int64_t ldw, int N, const void* bias,
+                               const int32_t* seg_len, int seg_rows, void* C, int64_t ldc,
+                               void* stream);
+
+/*
  * mha_attention -- the fused attention step for all heads: scores, scale,
  * mask, row softmax and weighted sum, written straight into the
  * concatenated layout (itwiki.kr "멀티 헤드 어텐션", table rows 헤드 분리

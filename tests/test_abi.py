@@ -171,6 +171,20 @@ def test_decode_and_linear_ex_reject_bad_arguments(lib):
         assert lin(ldr=32) == L.MHA_ERR_INVALID_ARG                 # residual row narrower than N
         assert lin(R=fake + (3 << 28) + 2) == L.MHA_ERR_INVALID_ARG # misaligned, overlapping C
         assert lin(R=fake + (3 << 28) + 64) == L.MHA_ERR_INVALID_ARG # partly overlaps C
+
+        def seg(**kw):
+            a = dict(A=fake, lda=64, M=512, K=64, W=fake + (1 << 28), ldw=64, N=64, bias=None,
+                     lens=fake + (2 << 28), seg_rows=256, C=fake + (3 << 28), ldc=64)
+            a.update(kw)
+            return L.mha_linear_segments(bf, a["A"], a["lda"], a["M"], a["K"], a["W"], a["ldw"],
+                                         a["N"], a["bias"], a["lens"], a["seg_rows"], a["C"], a["ldc"],
+                                         None, check=False)
+        assert seg(lens=None) == L.MHA_ERR_INVALID_ARG              # no segment lengths
+        assert seg(seg_rows=0) == L.MHA_ERR_INVALID_ARG
+        assert seg(seg_rows=300) == L.MHA_ERR_INVALID_ARG           # M not a multiple of it
+        assert seg(ldc=32) == L.MHA_ERR_INVALID_ARG                 # as mha_linear: C row < N
+        assert seg(A=fake + 2) == L.MHA_ERR_INVALID_ARG             # misaligned bf16 pointer
+        assert seg(M=0) == L.MHA_OK
     finally:
         L.mha_destroy(bf)
         L.mha_destroy(odd)

@@ -78,6 +78,28 @@ def test_linear_step(dtype, M, K, N, bias):
     assert_close(to_host(C), oracle.linear(A, W, b), dtype, f"linear {M}x{K}x{N}")
 
 
+def test_linear_segments_writes_every_needed_row():
+    """mha_linear_segments: the rows of each segment below its length rounded up to 128 equal
+    the oracle's projection (the rest may be skipped).  Segments of 700 rows straddle the
+    GEMM's 256-row blocks."""
+    lens = np.array([1, 300, 700, 129], dtype=np.int32)
+    seg, K, N = 700, 192, 384
+    A = wl.random_tensor((len(lens) * seg, K), seed=21)
+    W = wl.random_tensor((K, N), seed=22, scale=0.05)
+    b = wl.random_tensor((N,), seed=23, scale=0.1)
+    layer = Mha(64, 1, 64, dtype=torch.bfloat16)
+    C = torch.full((len(lens) * seg, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    layer.linear_segments(to_device(A, "bf16"), to_device(W, "bf16"), to_device(b, "bf16"),
+                          torch.from_numpy(lens).cuda(), seg, out=C)
+    torch.cuda.synchronize()
+    ref = oracle.linear(A, W, b)
+    got = to_host(C)
+    for i, L in enumerate(lens):
+        need = min((int(L) + 127) // 128 * 128, seg)
+        rows = slice(i * seg, i * seg + need)
+        assert_close(got[rows], ref[rows], "bf16", f"segment {i} (length {L})")
+
+
 def test_linear_strided_operands():
     """Row strides wider than the rows (a column block of W_qkv, as the
     cross-attention path uses)."""
@@ -266,6 +288,27 @@ def test_padding_rows_do_not_matter_and_runs_are_deterministic():
     x2["X_kv"] = xkv
     _, y2 = _run_forward(w, x2, layer)
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_cross_projection_leaves_unread_key_rows_alone(d):
+    """The key/value projection of cross-attention skips the 256-row blocks that lie past
+    every batch's key length (in whole 128-key tiles).  The workspace starts as NaN, so a
+    skipped row that the attention step did read would poison its batch's output.  T_kv is
+    not a multiple of 256, so row blocks straddle batches; the lengths cover 1 key, one
+    tile, a tile edge, and the whole sequence."""
+    w = wl.custom(f"skiprows{d}", B=5, T_q=70, T_kv=700, D=256, h=256 // d, d_k=d, cross=True,
+                  kv_len_range=(1, 700))
+    x = wl.make_inputs(w, seed=12)
+    x["kv_lengths"] = np.array([1, 127, 128, 300, 700], dtype=np.int32)
+    layer = _layer(w)
+    layer.ensure_workspace(w.B, w.T_q, w.T_kv).fill_(255)  # bf16 0xFFFF is a NaN
+    layer.status()  # the fill also hit the status word: read it to clear it
+    layer, y = _run_forward(w, x, layer)
+    assert layer.status() == _lib.MHA_OK
+    yh = to_host(y)
+    assert np.isfinite(yh).all()
+    assert_close(yh, _oracle_forward(w, x), "bf16", w.name)
 
 
 def test_output_guard_bands_untouched():

@@ -43,6 +43,7 @@ _SIGNATURES = {
                               _vp]),
     "mha_linear": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp]),
     "mha_linear_ex": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp, _i64, _vp]),
+    "mha_linear_segments": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i, _vp, _i64, _vp]),
     "mha_attention": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i64,
                            _vp]),
     "mha_attention_ex": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp,
@@ -159,6 +160,13 @@ def mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, R, ldr, C, ldc, stream,
     code = load().mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, R, ldr, C, ldc, stream)
     return _check("mha_linear_ex", code) if check else code
 
+
+
+def mha_linear_segments(handle, A, lda, M, K, W, ldw, N, bias, seg_len, seg_rows, C, ldc, stream,
+                        check: bool = True):
+    code = load().mha_linear_segments(handle, A, lda, M, K, W, ldw, N, bias, seg_len, seg_rows, C,
+                                      ldc, stream)
+    return _check("mha_linear_segments", code) if check else code
 
 def mha_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths, O, ldo,
                   stream, check: bool = True) -> int:

@@ -369,7 +369,11 @@ constexpr int P_HALF_B = 2 * P_B_CHUNK;            // 16 KB: 64 K-rows x this CT
 constexpr int P_A_BYTES = 2 * P_HALF_A;            // 32 KB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = 2 * P_HALF_B;            // 32 KB: this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + 1024;
+// Row-block list for a projection whose later rows of each segment are never read (the key /
+// value rows past a batch's key length): one flag byte and one list entry per 256-row block.
+constexpr int P_MLIST_MAX = 512;
+constexpr int P_LIST_BYTES = P_MLIST_MAX + 2 * P_MLIST_MAX + 16;
+constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + P_LIST_BYTES + 1024;
 
 static_assert(P_SMEM <= 232448, "shared memory budget (pair)");
 
@@ -379,7 +383,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmC,
                           const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* R,
-                          int64_t ldr, int M, int N, int K, int* status) {
+                          int64_t ldr, int M, int N, int K, int* status,
+                          const int32_t* __restrict__ seg_len, int seg_rows) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -397,6 +402,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t bar_drain = bar_tempty + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint8_t* mflag = gbase + (sBar + G_BAR_BYTES - base);         // [P_MLIST_MAX]
+    uint16_t* mlist = reinterpret_cast<uint16_t*>(mflag + P_MLIST_MAX);  // [P_MLIST_MAX]
+    int* mcount = reinterpret_cast<int*>(mlist + P_MLIST_MAX);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -404,10 +412,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const bool leader = rank == 0;
     const int pair = (int)(blockIdx.x >> 1);
     const int npairs = (int)(gridDim.x >> 1);
-    const int num_m = (M + 255) / 256;
+    const int num_m_all = (M + 255) / 256;
     const int num_n = (N + G_BN - 1) / G_BN;
-    const int num_tiles = num_m * num_n;
     const int num_k = (K + P_BK - 1) / P_BK;
+    const bool listed = seg_len != nullptr;  // the host guarantees num_m_all <= P_MLIST_MAX
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
@@ -437,6 +445,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     grid_dependency_wait();
     grid_launch_dependents();
 
+    // With segment lengths, only the 256-row blocks that hold a needed row are computed: row r
+    // of segment b = r / seg_rows is needed if r - b * seg_rows < seg_len[b] rounded up to a
+    // multiple of 128 (the reader loads whole 128-row tiles).  Every CTA builds the same list.
+    int num_m = num_m_all;
+    if (listed) {
+        for (int mb = (int)threadIdx.x; mb < num_m_all; mb += (int)blockDim.x) {
+            const int r0 = mb * 256;
+            const int r1 = min(r0 + 256, M);
+            bool need = false;
+            for (int b = r0 / seg_rows; b * seg_rows < r1 && !need; ++b) {
+                const int len = min(max(seg_len[b], 0), seg_rows);
+                const int upto = min((len + 127) / 128 * 128, seg_rows);
+                need = max(r0 - b * seg_rows, 0) < upto;
+            }
+            mflag[mb] = need ? 1 : 0;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int cnt = 0;
+            for (int c0 = 0; c0 < num_m_all; c0 += 32) {
+                const int mb = c0 + lane;
+                const bool f = mb < num_m_all && mflag[mb] != 0;
+                const uint32_t bal = __ballot_sync(0xffffffffu, f);
+                if (f) mlist[cnt + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)mb;
+                cnt += __popc(bal);
+            }
+            if (lane == 0) *mcount = cnt;
+        }
+        __syncthreads();
+        num_m = *mcount;
+    }
+    const int num_tiles = num_m * num_n;
+    // tile -> first row of its 256-row block (N fastest: see above)
+    auto tile_row0 = [&](int tile) { return (listed ? (int)mlist[tile / num_n] : tile / num_n) * 256; };
+
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs)
@@ -445,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                const int m0 = (tile / num_n) * 256 + (int)rank * 128;
+                const int m0 = tile_row0(tile) + (int)rank * 128;
                 const int nb = (tile % num_n) * G_BN + (int)rank * 128;
                 for (int kb = 0; kb < num_k; ++kb) {
                     if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
@@ -533,7 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         uint32_t bufsel = 0;
         int it = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
-            const int m0 = (tile / num_n) * 256 + (int)rank * 128;
+            const int m0 = tile_row0(tile) + (int)rank * 128;
             const int n0 = (tile % num_n) * G_BN;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -578,7 +621,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
                              const void* bias, const void* R, int64_t ldr, void* C, int64_t ldc,
-                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream) {
+                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream,
+                             const int32_t* seg_len, int seg_rows) {
     CUtensorMap tA, tW, tC;
     {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
@@ -631,9 +675,12 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         }
         const int pair_tiles = ((M + 255) / 256) * ((N + G_BN - 1) / G_BN);
         const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+        // the row-block list fits up to P_MLIST_MAX blocks; beyond that every row is computed
+        const bool listed = seg_len != nullptr && seg_rows >= 128 && (M + 255) / 256 <= P_MLIST_MAX;
         return launch_pdl(pair_kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream,
                           tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias),
-                          reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status);
+                          reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status,
+                          listed ? seg_len : nullptr, listed ? seg_rows : 0);
     }
     cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);

@@ -70,9 +70,13 @@ cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t
 
 // C = A W + bias (+ R) on tcgen05: bf16 operands, fp32 accumulation in TMEM, bf16 output.
 // Requires K, N, lda, ldw, ldc (and ldr) multiples of 8 and 16-byte aligned pointers.
+// seg_len (device int32 per segment of seg_rows rows) or null: rows of a segment at or past
+// its length rounded up to a multiple of 128 may be left unwritten (the key / value rows that
+// the attention kernels never load).
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
                              const void* bias, const void* R, int64_t ldr, void* C, int64_t ldc,
-                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream);
+                             int M, int N, int K, int num_sms, int* status, cudaStream_t stream,
+                             const int32_t* seg_len = nullptr, int seg_rows = 0);
 
 // Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v), grouped K/V heads
 // (h_kv divides h) and an optional gate G.  num_sms sizes the persistent grid of the d = 64

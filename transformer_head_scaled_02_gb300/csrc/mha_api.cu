@@ -145,9 +145,11 @@ int* status_ptr(const mha_s* m) { return m->ws ? reinterpret_cast<int*>(m->ws) :
 
 // ---------------------------------------------------------------- step launchers (validated)
 
+// seg_len / seg_rows: see launch_gemm_bf16 (rows the attention never reads may be skipped)
 mha_status run_linear(const mha_s* m, const void* A, int64_t lda, int M, int K, const void* W,
                       int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, void* C,
-                      int64_t ldc, cudaStream_t stream) {
+                      int64_t ldc, cudaStream_t stream, const int32_t* seg_len = nullptr,
+                      int seg_rows = 0) {
     cudaError_t err;
     if (m->dtype == MHA_F32) {
         err = mha::launch_gemm_f32(static_cast<const float*>(A), lda, static_cast<const float*>(W),
@@ -158,7 +160,7 @@ mha_status run_linear(const mha_s* m, const void* A, int64_t lda, int M, int K, 
         const mha_status st = query_sms(&sms);
         if (st != MHA_OK) return st;
         err = mha::launch_gemm_bf16(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, sms,
-                                    status_ptr(m), stream);
+                                    status_ptr(m), stream, seg_len, seg_rows);
     }
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -317,9 +319,14 @@ mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes) {
     return MHA_OK;
 }
 
-mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
-                         int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, void* C,
-                         int64_t ldc, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks shared by the projection entry points (M == 0 passes: nothing to do).
+mha_status check_linear(const mha_s* handle, const void* A, int64_t lda, int M, int K, const void* W,
+                        int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, const void* C,
+                        int64_t ldc) {
     if (handle == nullptr) return MHA_ERR_INVALID_ARG;
     if (M < 0 || K <= 0 || N <= 0) return MHA_ERR_INVALID_ARG;
     if (M == 0) return MHA_OK;
@@ -340,8 +347,30 @@ mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K,
     // the residual may be C itself (same rows), but not otherwise overlap it
     if (R && !(R == C && ldr == ldc) && overlaps(C, c_bytes, R, ((size_t)(M - 1) * ldr + N) * s))
         return MHA_ERR_INVALID_ARG;
+    return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
+                         int64_t ldw, int N, const void* bias, const void* R, int64_t ldr, void* C,
+                         int64_t ldc, void* stream) {
+    const mha_status st = check_linear(handle, A, lda, M, K, W, ldw, N, bias, R, ldr, C, ldc);
+    if (st != MHA_OK || M == 0) return st;
     return run_linear(handle, A, lda, M, K, W, ldw, N, bias, R, R ? ldr : 0, C, ldc,
                       static_cast<cudaStream_t>(stream));
+}
+
+mha_status mha_linear_segments(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
+                               int64_t ldw, int N, const void* bias, const int32_t* seg_len,
+                               int seg_rows, void* C, int64_t ldc, void* stream) {
+    if (seg_len == nullptr || seg_rows <= 0 || M % seg_rows != 0) return MHA_ERR_INVALID_ARG;
+    const mha_status st = check_linear(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc);
+    if (st != MHA_OK || M == 0) return st;
+    return run_linear(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc,
+                      static_cast<cudaStream_t>(stream), seg_len, seg_rows);
 }
 
 mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
@@ -445,8 +474,11 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
                             bqkv ? bqkv + g_off * s : nullptr, nullptr, 0, q + wd.q * s, qg, cs);
             if (st != MHA_OK) return st;
         }
+        // key/value rows past each batch's key length (in whole 128-key tiles) are never read
+        // by the attention step, so their projection may be skipped
         st = run_linear(m, X_kv, D, B * T_kv, (int)D, wqkv + k_off * s, ncols, (int)(wd.k + wd.v),
-                        bqkv ? bqkv + k_off * s : nullptr, nullptr, 0, kv, wd.k + wd.v, cs);
+                        bqkv ? bqkv + k_off * s : nullptr, nullptr, 0, kv, wd.k + wd.v, cs, kv_lengths,
+                        T_kv);
         if (st != MHA_OK) return st;
         st = run_attention(m, B, T_q, T_kv, q, qg, kv, wd.k + wd.v, kv + wd.k * s, wd.k + wd.v,
                            m->gated ? q + wd.q * s : nullptr, qg, causal, kv_lengths, ocat, hv, cs);

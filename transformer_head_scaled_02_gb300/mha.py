@@ -170,6 +170,27 @@ class Mha:
                            _ptr(out), out.stride(0), _stream())
         return out
 
+    def linear_segments(self, A: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor],
+                        seg_len: torch.Tensor, seg_rows: int,
+                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """C = A W + bias where only the rows that whole 128-row tiles up to each segment's
+        length need are guaranteed: the key/value projection of cross-attention with key
+        lengths seg_len (CUDA int32, one per segment of seg_rows rows)."""
+        M, K = A.shape
+        N = W.shape[1]
+        if out is None:
+            out = torch.empty((M, N), dtype=self.dtype, device=A.device)
+        for name, t in (("A", A), ("W", W), ("out", out)):
+            if not t.is_cuda or t.dtype != self.dtype or t.stride(1) != 1:
+                raise ValueError(f"{name} must be a row-major {self.dtype} CUDA matrix")
+        self._check("bias", bias, None if bias is None else (N,))
+        if seg_len.dtype != torch.int32 or not seg_len.is_cuda:
+            raise ValueError("seg_len must be a CUDA int32 tensor")
+        _lib.mha_linear_segments(self.handle, _ptr(A), A.stride(0), M, K, _ptr(W), W.stride(0), N,
+                                 _ptr(bias), _ptr(seg_len), seg_rows, _ptr(out), out.stride(0),
+                                 _stream())
+        return out
+
     def attention(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal: bool = False,
                   kv_lengths: Optional[torch.Tensor] = None,
                   out: Optional[torch.Tensor] = None,

@@ -4,7 +4,8 @@
 //   gemm_f32_kernel  C = A W + bias (+ R)   (itwiki.kr "멀티 헤드 어텐션", table rows 투영,
 //                    출력 투영; the residual R of iamjaehka13.blog "[Deep Learning 5]
 //                    Attention의 내부 계산", section 14)
-//   attn_f32_kernel  online-softmax attention for every head, any d_k, d_v <= 256, written
+//   attn_f32_tiled_kernel (the forward) and attn_f32_kernel (the decode step)
+//                    online-softmax attention for every head, any d_k, d_v <= 256, written
 //                    into the Concat layout (same page, 수식 and the shape table;
 //                    iamjaehka13.blog sections 9-10), with grouped K/V heads and the sigmoid
 //                    output gate (itwiki.kr, 추론 비용과 변형), and a decode mode in which
@@ -17,51 +18,103 @@
 namespace mha {
 namespace {
 
-constexpr int F_BM = 64, F_BN = 64, F_BK = 16;
+constexpr int F_BN = 64;
 
-// 64x64 output tile per 256-thread block, 4x4 outputs per thread; the K loop runs in
-// order (k = 0, 1, ...) with one FFMA per product.
-__global__ void __launch_bounds__(256)
+// BM x 64 output tile per block of BM * 4 threads, 4x4 outputs per thread (rows 4 ty..,
+// columns 4 tx..), K consumed in slices of BK.  Shared-memory tiles are double-buffered: the
+// next slice is loaded from global memory into registers while the current one is
+// multiplied, then stored to the other buffer, one barrier per slice.  A is staged
+// transposed (As[k][m]) so that both operands of a product step are one 16-byte shared load
+// each.  The K loop runs in order (k = 0, 1, ...) with one FFMA per product.  VEC: A and W
+// 16-byte aligned with row strides a multiple of 4 floats, so that four consecutive elements
+// of a row are one 16-byte global load.
+template <int BM, int BK, bool VEC>
+__global__ void __launch_bounds__(BM * 4)
     gemm_f32_kernel(const float* __restrict__ A, int64_t lda, const float* __restrict__ W,
                     int64_t ldw, const float* __restrict__ bias, const float* R, int64_t ldr,
                     float* C, int64_t ldc, int M, int N, int K) {
-    __shared__ float As[F_BK][F_BM + 4];  // As[k][m]
-    __shared__ float Ws[F_BK][F_BN + 4];  // Ws[k][n]
-    const int tx = threadIdx.x & 15;
-    const int ty = threadIdx.x >> 4;
-    const int m0 = blockIdx.y * F_BM;
+    constexpr int THREADS = BM * 4;
+    constexpr int NA = BM * BK / 4 / THREADS;  // 4-element pieces of A per thread and slice
+    constexpr int NW = BK * F_BN / 4 / THREADS;
+    static_assert(NA >= 1 && NW >= 1, "slice smaller than the block");
+    __shared__ __align__(16) float As[2][BK][BM + 4];     // As[buf][k][m]
+    __shared__ __align__(16) float Ws[2][BK][F_BN + 4];   // Ws[buf][k][n]
+    const int tid = (int)threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * F_BN;
+    float ra[NA][4], rw[NW][4];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int c = 0; c < NA; ++c) {
+            const int idx = tid + c * THREADS;
+            const int gm = m0 + idx / (BK / 4), gk = k0 + (idx % (BK / 4)) * 4;
+            if (VEC && gm < M && gk + 3 < K) {
+                const float4 v = *reinterpret_cast<const float4*>(A + (int64_t)gm * lda + gk);
+                ra[c][0] = v.x; ra[c][1] = v.y; ra[c][2] = v.z; ra[c][3] = v.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    ra[c][i] = (gm < M && gk + i < K) ? A[(int64_t)gm * lda + gk + i] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < NW; ++c) {
+            const int idx = tid + c * THREADS;
+            const int gw = k0 + idx / 16, gn = n0 + (idx % 16) * 4;
+            if (VEC && gw < K && gn + 3 < N) {
+                const float4 v = *reinterpret_cast<const float4*>(W + (int64_t)gw * ldw + gn);
+                rw[c][0] = v.x; rw[c][1] = v.y; rw[c][2] = v.z; rw[c][3] = v.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    rw[c][i] = (gw < K && gn + i < N) ? W[(int64_t)gw * ldw + gn + i] : 0.f;
+            }
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int c = 0; c < NA; ++c) {
+            const int idx = tid + c * THREADS;
+            const int r = idx / (BK / 4), k4 = (idx % (BK / 4)) * 4;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) As[buf][k4 + i][r] = ra[c][i];
+        }
+#pragma unroll
+        for (int c = 0; c < NW; ++c) {
+            const int idx = tid + c * THREADS;
+            *reinterpret_cast<float4*>(&Ws[buf][idx / 16][(idx % 16) * 4]) =
+                make_float4(rw[c][0], rw[c][1], rw[c][2], rw[c][3]);
+        }
+    };
+
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    for (int k0 = 0; k0 < K; k0 += F_BK) {
+    load(0);
+    store(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < K; k0 += BK) {
+        const bool more = k0 + BK < K;
+        if (more) load(k0 + BK);  // in flight while this slice is multiplied
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int idx = threadIdx.x + p * 256;
-            const int r = idx >> 4, c = idx & 15;  // A: 64 rows x 16 k
-            const int gm = m0 + r, gk = k0 + c;
-            As[c][r] = (gm < M && gk < K) ? A[(int64_t)gm * lda + gk] : 0.f;
-            const int wr = idx >> 6, wc = idx & 63;  // W: 16 k x 64 cols
-            const int wk = k0 + wr, wn = n0 + wc;
-            Ws[wr][wc] = (wk < K && wn < N) ? W[(int64_t)wk * ldw + wn] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < F_BK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tx * 4 + j];
+        for (int kk = 0; kk < BK; ++kk) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&Ws[buf][kk][tx * 4]);
+            const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
+        if (more) store(buf ^ 1);  // the other buffer was last read before the previous barrier
         __syncthreads();
+        buf ^= 1;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -75,6 +128,20 @@ __global__ void __launch_bounds__(256)
                     acc[i][j] + (bias ? bias[gn] : 0.f) + (R ? R[(int64_t)gm * ldr + gn] : 0.f);
         }
     }
+}
+
+template <int BM, int BK>
+cudaError_t launch_gemm_f32_cfg(const float* A, int64_t lda, const float* W, int64_t ldw,
+                                const float* bias, const float* R, int64_t ldr, float* C,
+                                int64_t ldc, int M, int N, int K, cudaStream_t stream) {
+    const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + BM - 1) / BM));
+    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0) &&
+                     lda % 4 == 0 && ldw % 4 == 0;
+    if (vec)
+        gemm_f32_kernel<BM, BK, true><<<grid, BM * 4, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+    else
+        gemm_f32_kernel<BM, BK, false><<<grid, BM * 4, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+    return cudaGetLastError();
 }
 
 constexpr int FA_BQ = 16;      // query rows per block (4 per warp)
@@ -200,14 +267,226 @@ __global__ void __launch_bounds__(FA_THREADS)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Tiled fp32 attention (the forward; the decode step keeps the kernel above): one block =
+// BQ = 16 RQ query rows of one (batch, head), 256 threads, key tiles of 64.  Per key tile the
+// block forms the BQ x 64 score tile as a small matrix product (thread = RQ rows x 4 keys),
+// masks it, updates the online softmax (row maximum and sum over the 16 threads sharing the
+// rows, by shuffles), stages P in shared memory and adds P V to its RQ x (4 CV) outputs
+// (columns c*64 + 4 tx + i).  Q and K are staged transposed (Qs[e][q], Ks[e][j]) so that a
+// product step reads 16 bytes of each; V and P row-major.  Causal: key tiles past the block's
+// last row are skipped.  d_k any size, d_v <= 64 CV.
+constexpr int FT_BK = 64;
+constexpr int FT_THREADS = 256;
+constexpr int FT_PAD = 4;  // row padding of the transposed and P tiles (floats)
+
+__host__ __device__ constexpr int ft_bq(int RQ) { return 16 * RQ; }
+
+template <int RQ, int CV>
+__global__ void __launch_bounds__(FT_THREADS)
+    attn_f32_tiled_kernel(const float* __restrict__ Q, int64_t ldq, const float* __restrict__ K,
+                          int64_t ldk, const float* __restrict__ V, int64_t ldv,
+                          const float* __restrict__ G, int64_t ldg, float* __restrict__ O,
+                          int64_t ldo, int h, int h_kv, int T_q, int T_kv, int dk, int dv,
+                          int causal, const int32_t* __restrict__ kv_lengths, float scale,
+                          int* status) {
+    constexpr int BQ = ft_bq(RQ);
+    constexpr int QS = BQ + FT_PAD;      // row stride of Qs
+    constexpr int KS = FT_BK + FT_PAD;   // row stride of Ks and Ps
+    constexpr int VS = 64 * CV;          // row stride of Vs
+    extern __shared__ __align__(16) float fsm[];
+    const int dk4 = (dk + 3) & ~3;
+    float* Qs = fsm;                 // [dk4][QS]
+    float* Ks = Qs + dk4 * QS;       // [dk4][KS]
+    float* Vs = Ks + dk4 * KS;       // [FT_BK][VS]
+    float* Ps = Vs + FT_BK * VS;     // [BQ][KS]
+    const int tid = (int)threadIdx.x;
+    const int tx = tid & 15;  // keys 4 tx .. 4 tx + 3 of a score tile; output columns c*64 + 4 tx ..
+    const int ty = tid >> 4;  // rows RQ ty .. RQ ty + RQ - 1
+    const int bh = blockIdx.x;
+    const int b = bh / h, head = bh - b * h;
+    const int kvh = head / (h / h_kv);
+    const int qb = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;  // long blocks first
+    const int q0 = qb * BQ;
+    const int L = kv_lengths ? kv_lengths[b] : T_kv;
+    if (L < 1 || L > T_kv) {
+        if (tid == 0) record_status(status, kStatusBadLength);
+        for (int i = tid; i < BQ * dv; i += FT_THREADS) {
+            const int r = i / dv, e = i - r * dv;
+            if (q0 + r < T_q) O[((int64_t)b * T_q + q0 + r) * ldo + (int64_t)head * dv + e] = NAN;
+        }
+        return;
+    }
+    // Q tile, transposed; rows past T_q and columns past d_k are zero
+    for (int i = tid; i < BQ * (dk4 / 4); i += FT_THREADS) {
+        const int q = i % BQ, e4 = (i / BQ) * 4;
+        const int t = q0 + q;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            Qs[(e4 + c) * QS + q] = (t < T_q && e4 + c < dk)
+                                        ? Q[((int64_t)b * T_q + t) * ldq + (int64_t)head * dk + e4 + c] : 0.f;
+    }
+    int kv_end = L;
+    if (causal && kv_end > q0 + BQ) kv_end = q0 + BQ;
+
+    float m[RQ], l[RQ], o[RQ][4 * CV];
+#pragma unroll
+    for (int r = 0; r < RQ; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4 * CV; ++u) o[r][u] = 0.f;
+    }
+    for (int kt0 = 0; kt0 < kv_end; kt0 += FT_BK) {
+        __syncthreads();  // the previous tile's K, V and P are no longer read
+        for (int i = tid; i < FT_BK * (dk4 / 4); i += FT_THREADS) {
+            const int j = i % FT_BK, e4 = (i / FT_BK) * 4;
+            const int key = kt0 + j;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                Ks[(e4 + c) * KS + j] = (key < T_kv && e4 + c < dk)
+                                            ? K[((int64_t)b * T_kv + key) * ldk + (int64_t)kvh * dk + e4 + c] : 0.f;
+        }
+        for (int i = tid; i < FT_BK * (VS / 4); i += FT_THREADS) {
+            const int j = i / (VS / 4), e4 = (i - j * (VS / 4)) * 4;
+            const int key = kt0 + j;
+            float v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                v[c] = (key < T_kv && e4 + c < dv) ? V[((int64_t)b * T_kv + key) * ldv + (int64_t)kvh * dv + e4 + c] : 0.f;
+            *reinterpret_cast<float4*>(&Vs[j * VS + e4]) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        __syncthreads();
+        // scores of this thread's RQ rows x 4 keys
+        float sc[RQ][4];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[r][c] = 0.f;
+#pragma unroll 4
+        for (int e = 0; e < dk4; ++e) {
+            float a[RQ];
+            if constexpr (RQ == 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(&Qs[e * QS + ty * 4]);
+                a[0] = a4.x; a[1] = a4.y; a[2] = a4.z; a[3] = a4.w;
+            } else {
+                const float2 a2 = *reinterpret_cast<const float2*>(&Qs[e * QS + ty * RQ]);
+                a[0] = a2.x; a[1] = a2.y;
+            }
+            const float4 k4 = *reinterpret_cast<const float4*>(&Ks[e * KS + tx * 4]);
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int r = 0; r < RQ; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[r][c] = fmaf(a[r], kk[c], sc[r][c]);
+        }
+        // mask, online softmax (the 16 threads of a half-warp share their rows)
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) {
+            const int t = q0 + ty * RQ + r;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int key = kt0 + tx * 4 + c;
+                const bool visible = key < L && !(causal && key > t);
+                sc[r][c] = visible ? sc[r][c] * scale : -INFINITY;
+                tmax = fmaxf(tmax, sc[r][c]);
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+            const float m_new = fmaxf(m[r], tmax);
+            float psum = 0.f;
+            if (m_new == -INFINITY) {  // nothing visible to this row yet
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[r][c] = 0.f;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    sc[r][c] = expf(sc[r][c] - m_new);  // masked: exp(-inf) = 0
+                    psum += sc[r][c];
+                }
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+            const float alpha = m_new == -INFINITY ? 1.f : expf(m[r] - m_new);  // 0 when m = -inf
+            l[r] = l[r] * alpha + psum;
+#pragma unroll
+            for (int u = 0; u < 4 * CV; ++u) o[r][u] *= alpha;
+            m[r] = m_new;
+            *reinterpret_cast<float4*>(&Ps[(ty * RQ + r) * KS + tx * 4]) =
+                make_float4(sc[r][0], sc[r][1], sc[r][2], sc[r][3]);
+        }
+        __syncthreads();
+        // O += P V over the tile's keys, four at a time
+        const int nk = min(FT_BK, kv_end - kt0);
+        for (int j4 = 0; j4 < nk; j4 += 4) {
+            float p[RQ][4];
+#pragma unroll
+            for (int r = 0; r < RQ; ++r) {
+                const float4 p4 = *reinterpret_cast<const float4*>(&Ps[(ty * RQ + r) * KS + j4]);
+                p[r][0] = p4.x; p[r][1] = p4.y; p[r][2] = p4.z; p[r][3] = p4.w;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                for (int c = 0; c < CV; ++c) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(&Vs[(j4 + jj) * VS + c * 64 + tx * 4]);
+                    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                    for (int r = 0; r < RQ; ++r)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) o[r][c * 4 + u] = fmaf(p[r][jj], v[u], o[r][c * 4 + u]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RQ; ++r) {
+        const int t = q0 + ty * RQ + r;
+        if (t >= T_q) continue;
+        const float inv = 1.f / l[r];
+#pragma unroll
+        for (int c = 0; c < CV; ++c)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = c * 64 + tx * 4 + u;
+                if (e >= dv) continue;
+                float y = o[r][c * 4 + u] * inv;
+                if (G != nullptr) y *= 1.f / (1.f + expf(-G[((int64_t)b * T_q + t) * ldg + (int64_t)head * dv + e]));
+                O[((int64_t)b * T_q + t) * ldo + (int64_t)head * dv + e] = y;
+            }
+    }
+}
+
+template <int RQ, int CV>
+cudaError_t launch_attn_f32_tiled(const float* Q, int64_t ldq, const float* K, int64_t ldk,
+                                  const float* V, int64_t ldv, const float* G, int64_t ldg, float* O,
+                                  int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d_k,
+                                  int d_v, int causal, const int32_t* kv_lengths, int* status,
+                                  cudaStream_t stream) {
+    constexpr int BQ = ft_bq(RQ);
+    const int dk4 = (d_k + 3) & ~3;
+    const size_t smem = sizeof(float) * ((size_t)dk4 * (BQ + FT_PAD) + (size_t)dk4 * (FT_BK + FT_PAD) +
+                                         (size_t)FT_BK * 64 * CV + (size_t)BQ * (FT_BK + FT_PAD));
+    if (smem > 232448) return cudaErrorInvalidValue;
+    auto kernel = attn_f32_tiled_kernel<RQ, CV>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const float scale = (float)(1.0 / sqrt((double)d_k));
+    const dim3 grid((unsigned)(B * h), (unsigned)((T_q + BQ - 1) / BQ));
+    kernel<<<grid, FT_THREADS, smem, stream>>>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, h, h_kv, T_q,
+                                               T_kv, d_k, d_v, causal, kv_lengths, scale, status);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t ldw,
                             const float* bias, const float* R, int64_t ldr, float* C, int64_t ldc,
                             int M, int N, int K, cudaStream_t stream) {
-    const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + F_BM - 1) / F_BM));
-    gemm_f32_kernel<<<grid, 256, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
-    return cudaGetLastError();
+    // 64-row tiles, 32-wide K slices: measured best of 64/32/16 rows x 16/32 K on the
+    // 1024 x 512 x {1536, 512} projections of the fp32 causal workload
+    return launch_gemm_f32_cfg<64, 32>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, stream);
 }
 
 cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,
@@ -215,6 +494,19 @@ cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t
                             int64_t ldo, int B, int h, int h_kv, int T_q, int T_kv, int d_k, int d_v,
                             int causal, int decode, const int32_t* kv_lengths, int* status,
                             cudaStream_t stream) {
+    if (!decode && d_v <= 256) {
+        // the forward: tiled kernel; 32-row blocks when 64-row ones would not fill the GPU twice
+        const bool small = (int64_t)B * h * ((T_q + 63) / 64) < 256;
+        const int cv = (d_v + 63) / 64;
+#define MHA_FT(RQ, CV)                                                                                  \
+    if ((small ? 2 : 4) == RQ && cv == CV)                                                              \
+        return launch_attn_f32_tiled<RQ, CV>(Q, ldq, K, ldk, V, ldv, G, ldg, O, ldo, B, h, h_kv, T_q, \
+                                             T_kv, d_k, d_v, causal, kv_lengths, status, stream);
+        MHA_FT(2, 1) MHA_FT(2, 2) MHA_FT(2, 3) MHA_FT(2, 4)
+        MHA_FT(4, 1) MHA_FT(4, 2) MHA_FT(4, 3) MHA_FT(4, 4)
+#undef MHA_FT
+    }
+    // the decode step (a few new rows over a long cache): 16-row blocks
     const size_t smem = sizeof(float) * (size_t)(FA_BQ * d_k + FA_BKEY * (d_k + 1) + FA_BKEY * d_v);
     cudaError_t err = cudaFuncSetAttribute(attn_f32_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -346,14 +346,15 @@ def run_ours(args):
         torch.cuda.synchronize()
         launch_ms = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
                      for i, n in enumerate(["q_proj", "kv_proj", "attention", "out_proj"])}
-        per_kernel = {"qkv_proj": launch_ms["q_proj"] + launch_ms["kv_proj"],
-                      "attention": launch_ms["attention"], "out_proj": launch_ms["out_proj"]}
+        per_kernel = launch_ms
+        # FLOPs per launch; with key lengths the kernels visit only the L_b valid keys of each
+        # batch (the key/value projection skips whole 256-row blocks past them)
+        L = float(w.B * w.T_kv)
         if x["kv_lengths"] is not None:
             import numpy as np
-            # the kernels visit only the L_b valid keys of each batch
             L = float(np.sum(np.asarray(x["kv_lengths"], dtype=np.float64)))
-            sf = dict(sf, attention=2.0 * w.h * w.T_q * L * (w.d_k + w.d_v) * (0.5 if w.causal else 1.0),
-                      qkv_proj=2.0 * w.D * (w.B * w.T_q * hq + L * (hk + hv)))
+        sf = dict(sf, q_proj=2.0 * w.D * w.B * w.T_q * hq, kv_proj=2.0 * w.D * L * (hk + hv),
+                  attention=2.0 * w.h * w.T_q * L * (w.d_k + w.d_v) * (0.5 if w.causal else 1.0))
 
     # ---------------- end to end through the public API, host buffers in and out
     xh = d["X_q"].cpu().pin_memory()
@@ -399,8 +400,6 @@ def run_ours(args):
                     "per_kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
                     "per_kernel_frac_of_peak": {k: round(sf[k] / (v / 1e3) / 1e12 / peak, 4)
                                                 for k, v in per_kernel.items()}}
-        if w.cross:
-            roofline["per_launch_ms"] = {k: round(v, 4) for k, v in launch_ms.items()}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,

@@ -392,11 +392,19 @@ def run_ours(args):
         if w.dtype == "f32":
             src = "simt_f32.cu"
         ach = sf[top] / (per_kernel[top] / 1e3) / 1e12
-        peak = pk["bf16_tflops"]
-        roofline = {"kernel": top, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+        if w.dtype == "f32":
+            # fp32 runs as FFMA on the CUDA cores: SMs x 128 fp32 lanes x 2 FLOP x max SM clock
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            mhz = float(pk.get("sm_max_mhz", 2070.0))
+            peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 1)
+            bound, peak_source = "alu", f"derived fp32 FFMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
+        else:
+            peak = pk["bf16_tflops"]
+            bound, peak_source = "tensor", f"{pk_src} bf16 dense (burst)"
+        roofline = {"kernel": top, "bound": bound, "achieved": round(ach, 1), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                     "traffic": recorded_traffic(top, w.name, src),
-                    "peak_source": f"{pk_src} bf16 dense (burst)",
+                    "peak_source": peak_source,
                     "per_kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
                     "per_kernel_frac_of_peak": {k: round(sf[k] / (v / 1e3) / 1e12 / peak, 4)
                                                 for k, v in per_kernel.items()}}

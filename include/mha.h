@@ -147,6 +147,22 @@ mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, i
                        int causal, const int32_t* kv_lengths, void* out, void* stream);
 
 /*
+ * mha_forward_checked -- mha_forward that first validates the key lengths on the host, for
+ * debugging and for callers that want an invalid length reported before any work instead of
+ * NaN rows plus a device status.
+ *   kv_lengths_host  host int32[B], a copy of the device array kv_lengths (the caller keeps
+ *                    the two equal; both NULL, or both non-NULL, else MHA_ERR_INVALID_ARG).
+ * Every L_b must lie in [1, T_kv] (molayo1419.me "MHA란 무엇인가?", pitfall 3: a row with no
+ * visible key has no softmax); otherwise MHA_ERR_BAD_LENGTH is returned and nothing is launched.
+ * All other arguments, checks and behaviour are those of mha_forward.  Reads only host memory
+ * before launching; asynchronous like mha_forward.
+ */
+mha_status mha_forward_checked(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q,
+                               int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                               const void* b_o, int causal, const int32_t* kv_lengths,
+                               const int32_t* kv_lengths_host, void* out, void* stream);
+
+/*
  * mha_forward_ex -- mha_forward for a handle of any mha_create_ex shape (W_qkv with the
  * column blocks described there), plus an optional residual:
  *   residual  (B, T_q, D) or NULL; added to the output in the output projection's epilogue,

@@ -207,6 +207,27 @@ def test_forward_host_workspace_layout(lib):
         L.mha_destroy(hdl)
 
 
+def test_forward_checked_validates_host_lengths_before_any_launch(lib):
+    import numpy as np
+    hdl = L.mha_create(256, 4, 64, 64, L.MHA_BF16)
+    fake = 1 << 40  # never dereferenced: every call below returns before any launch
+    try:
+        def fwd(lens_dev, lens_host, T_kv=100):
+            return L.mha_forward_checked(hdl, fake, fake + (1 << 30), 3, 50, T_kv, fake + (2 << 30), None,
+                                         fake + (3 << 30), None, 0, lens_dev, lens_host,
+                                         fake + (4 << 30), None, check=False)
+        good = np.array([1, 100, 37], dtype=np.int32)
+        assert fwd(fake + (5 << 30), np.array([0, 100, 37], dtype=np.int32)) == L.MHA_ERR_BAD_LENGTH
+        assert fwd(fake + (5 << 30), np.array([1, 101, 37], dtype=np.int32)) == L.MHA_ERR_BAD_LENGTH
+        assert fwd(fake + (5 << 30), None) == L.MHA_ERR_INVALID_ARG   # device lengths, no host copy
+        assert fwd(None, good) == L.MHA_ERR_INVALID_ARG                # host copy, no device lengths
+        # valid lengths: on to mha_forward, which finds no workspace attached
+        assert fwd(fake + (5 << 30), good) == L.MHA_ERR_WORKSPACE
+        assert fwd(None, None) == L.MHA_ERR_WORKSPACE
+    finally:
+        L.mha_destroy(hdl)
+
+
 def test_forward_host_rejects_bad_arguments_before_any_copy(lib):
     hdl = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
     fake = 1 << 40  # never dereferenced: every call below is rejected first

@@ -311,6 +311,31 @@ def test_cross_projection_leaves_unread_key_rows_alone(d):
     assert_close(yh, _oracle_forward(w, x), "bf16", w.name)
 
 
+def test_forward_checked_matches_forward_and_rejects_bad_lengths():
+    w = wl.custom("checked", B=3, T_q=40, T_kv=300, D=256, h=4, d_k=64, cross=True,
+                  kv_len_range=(1, 300))
+    x = wl.make_inputs(w, seed=13)
+    layer, y = _run_forward(w, x)
+    d = {k: to_device(v, w.dtype) for k, v in x.items() if k != "kv_lengths"}
+    kvl = torch.from_numpy(x["kv_lengths"]).cuda()
+    y2 = torch.empty_like(y)
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (layer.handle, d["X_q"].data_ptr(), d["X_kv"].data_ptr(), w.B, w.T_q, w.T_kv,
+            d["W_qkv"].data_ptr(), d["b_qkv"].data_ptr(), d["W_o"].data_ptr(), d["b_o"].data_ptr(), 0,
+            kvl.data_ptr())
+    assert _lib.mha_forward_checked(*args, x["kv_lengths"], y2.data_ptr(), stream) == _lib.MHA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    bad = x["kv_lengths"].copy()
+    bad[1] = 0
+    y3 = torch.full_like(y, 7.0)
+    code = _lib.mha_forward_checked(*args, bad, y3.data_ptr(), stream, check=False)
+    torch.cuda.synchronize()
+    assert code == _lib.MHA_ERR_BAD_LENGTH
+    assert (y3 == 7.0).all()  # nothing was launched
+    assert layer.status() == _lib.MHA_OK
+
+
 def test_output_guard_bands_untouched():
     w = wl.custom("guard", B=2, T_q=131, D=256, h=4, d_k=64, causal=True)
     x = wl.make_inputs(w, seed=7)

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "mha_workspace_size": (_sz, [_vp, _i, _i, _i]),
     "mha_set_workspace": (_i, [_vp, _vp, _sz]),
     "mha_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp]),
+    "mha_forward_checked": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
     "mha_forward_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
     "mha_forward_host_workspace_size": (_sz, [_vp, _i, _i, _i, _i]),
     "mha_forward_host": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i,
@@ -130,6 +131,19 @@ def mha_forward(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal,
     code = load().mha_forward(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o,
                               int(causal), kv_lengths, out, stream)
     return _check("mha_forward", code) if check else code
+
+
+def mha_forward_checked(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal,
+                        kv_lengths, kv_lengths_host, out, stream, check: bool = True) -> int:
+    """kv_lengths_host: a host int32 array (numpy) equal to the device kv_lengths, or None."""
+    hp = None
+    if kv_lengths_host is not None:
+        import numpy as np
+        arr = np.ascontiguousarray(kv_lengths_host, dtype=np.int32)
+        hp = arr.ctypes.data_as(ctypes.c_void_p)
+    code = load().mha_forward_checked(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o,
+                                      int(causal), kv_lengths, hp, out, stream)
+    return _check("mha_forward_checked", code) if check else code
 
 
 def mha_forward_ex(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal, kv_lengths,

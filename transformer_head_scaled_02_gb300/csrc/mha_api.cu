@@ -487,6 +487,18 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
     return run_linear(m, ocat, hv, B * T_q, (int)hv, W_o, D, (int)D, b_o, residual, D, out, D, cs);
 }
 
+mha_status mha_forward_checked(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q,
+                               int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                               const void* b_o, int causal, const int32_t* kv_lengths,
+                               const int32_t* kv_lengths_host, void* out, void* stream) {
+    if ((kv_lengths == nullptr) != (kv_lengths_host == nullptr)) return MHA_ERR_INVALID_ARG;
+    if (kv_lengths_host != nullptr)
+        for (int b = 0; b < B; ++b)
+            if (kv_lengths_host[b] < 1 || kv_lengths_host[b] > T_kv) return MHA_ERR_BAD_LENGTH;
+    return mha_forward(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal, kv_lengths, out,
+                       stream);
+}
+
 mha_status mha_forward(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
                        const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
                        int causal, const int32_t* kv_lengths, void* out, void* stream) {

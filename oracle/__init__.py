@@ -90,6 +90,10 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                 ctypes.c_int, _ip, _ip, ctypes.c_int, _dp, ctypes.c_int]
+            lib.oracle_mha_forward_rounded.restype = ctypes.c_int
+            lib.oracle_mha_forward_rounded.argtypes = lib.oracle_mha_forward_ex.argtypes
+            lib.oracle_round_bf16.restype = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_decode.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -183,14 +187,21 @@ def proj_width(h: int, d_k: int, d_v: int, h_kv=None, gated: bool = False) -> in
     return h * d_k + h_kv * d_k + h_kv * d_v + (h * d_v if gated else 0)
 
 
+def round_bf16(x: float) -> float:
+    """x rounded to the nearest bfloat16 value, ties to even (the oracle's own rounding)."""
+    return float(_load().oracle_round_bf16(float(x)))
+
+
 def mha_forward(Xq, Wqkv, bqkv, Wo, bo, h: int, d_k: int, d_v: int, Xkv=None,
                 causal: bool = False, kv_lengths=None, rows=None, nthreads: int = 0,
-                h_kv=None, gated: bool = False, residual=None):
+                h_kv=None, gated: bool = False, residual=None, round_bf16: bool = False):
     """The whole forward.  Xq (B,Tq,D); Xkv (B,Tkv,D) or None (self-attention);
     Wqkv (D, proj_width(...)) with column blocks [Q|K|V(|G)]; Wo (h*d_v, D).
     h_kv: K/V heads (default h); gated: sigmoid output gate from the G block;
     residual: (B,Tq,D) added to Y.  rows: optional query-row indices (shared by every
-    batch) to compute.  Returns Y (B, n_out, D) in fp64."""
+    batch) to compute.  round_bf16: the secondary diagnostic mode that rounds to bf16
+    where the bf16 GPU path stores values (Q/K/V/G, the softmax weights entering the
+    weighted sum, the attention output, Y).  Returns Y (B, n_out, D) in fp64."""
     lib = _load()
     Xq = _f64(Xq)
     Xkv = _f64(Xkv)
@@ -210,7 +221,8 @@ def mha_forward(Xq, Wqkv, bqkv, Wo, bo, h: int, d_k: int, d_v: int, Xkv=None,
     rws = _i32(rows)
     n_out = Tq if rws is None else len(rws)
     Y = np.empty((B, n_out, D), dtype=np.float64)
-    rc = lib.oracle_mha_forward_ex(B, Tq, Tkv, D, h, h_kv, d_k, d_v, int(bool(gated)), _ptr(Xq),
+    fn = lib.oracle_mha_forward_rounded if round_bf16 else lib.oracle_mha_forward_ex
+    rc = fn(B, Tq, Tkv, D, h, h_kv, d_k, d_v, int(bool(gated)), _ptr(Xq),
                                    _ptr(Xkv), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), _ptr(R),
                                    int(bool(causal)), _iptr(kvl), _iptr(rws),
                                    0 if rws is None else len(rws), _ptr(Y), nthreads)

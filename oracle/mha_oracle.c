@@ -54,6 +54,13 @@
  *     L_b < T_q or L_b > T_max is invalid and gives NaN rows.
  *
  * Precision: every operation is IEEE fp64; exp is libm exp().
+ *
+ * Rounded mode (oracle_mha_forward_rounded, a secondary diagnostic): the same steps, with the
+ * values the bf16 GPU path stores rounded to bf16 (round to nearest, ties to even) where it
+ * stores them -- the projections Q, K, V (and the gate pre-activations), the unnormalised
+ * softmax weights exp(s_j - m) that enter the weighted sum (their sum, the denominator, is
+ * not rounded), the attention output after the gate, and Y.  The pass/fail reference stays
+ * the unrounded forward.
  * Threads: OpenMP over independent output rows / (batch, head) pairs; the
  * arithmetic done for any one output element does not depend on the thread
  * count.
@@ -75,6 +82,23 @@ static void set_threads(int nthreads) {
 #else
     (void)nthreads;
 #endif
+}
+
+/*
+ * x rounded to the nearest bfloat16 value (8 significant bits), ties to even: with
+ * x = m * 2^e and 0.5 <= |m| < 1, keep m * 2^8 rounded to an integer (nearbyint rounds to
+ * nearest, ties to even, in the default rounding mode).  Values below the bf16 normal range
+ * (2^-126) are rounded as if it extended further; none arise here.
+ */
+double oracle_round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    const double m = frexp(x, &e);
+    return ldexp(nearbyint(ldexp(m, 8)), e - 8);
+}
+
+static void round_all(double* a, long n) {
+    for (long i = 0; i < n; ++i) a[i] = oracle_round_bf16(a[i]);
 }
 
 int oracle_max_threads(void) {
@@ -136,13 +160,13 @@ int oracle_linear(long M, long K, long N,
  *   o_e = sum_j w_j v_je
  * The whole score row is materialised before the softmax.
  */
-int oracle_attention_grouped(int B, int Tq, int Tkv, int h, int h_kv, int dk, int dv,
-                             const double* Q, long ldq,
-                             const double* K, long ldk,
-                             const double* V, long ldv,
-                             int causal, const int* kv_lengths,
-                             const int* rows, int n_rows,
-                             double* O, long ldo, double* P, int nthreads) {
+static int attention_impl(int B, int Tq, int Tkv, int h, int h_kv, int dk, int dv,
+                          const double* Q, long ldq,
+                          const double* K, long ldk,
+                          const double* V, long ldv,
+                          int causal, const int* kv_lengths,
+                          const int* rows, int n_rows,
+                          double* O, long ldo, double* P, int nthreads, int round_p) {
     if (B < 0 || Tq < 0 || Tkv < 0 || h <= 0 || dk <= 0 || dv <= 0) return ORACLE_BAD_ARG;
     if (h_kv <= 0 || h % h_kv != 0) return ORACLE_BAD_ARG;
     if (!Q || !K || !V || !O) return ORACLE_BAD_ARG;
@@ -198,7 +222,8 @@ int oracle_attention_grouped(int B, int Tq, int Tkv, int h, int h_kv, int dk, in
                 s[j] = exp(s[j] - m);
                 sum += s[j];
             }
-            for (int j = 0; j < Tkv; ++j) s[j] = s[j] / sum;
+            /* rounded mode: the weights enter the weighted sum as bf16, the sum does not */
+            for (int j = 0; j < Tkv; ++j) s[j] = (round_p ? oracle_round_bf16(s[j]) : s[j]) / sum;
             if (prow) memcpy(prow, s, sizeof(double) * (size_t)Tkv);
             /* weighted sum of values */
             for (int e = 0; e < dv; ++e) o[e] = 0.0;
@@ -211,6 +236,17 @@ int oracle_attention_grouped(int B, int Tq, int Tkv, int h, int h_kv, int dk, in
         free(s);
     }
     return status;
+}
+
+int oracle_attention_grouped(int B, int Tq, int Tkv, int h, int h_kv, int dk, int dv,
+                             const double* Q, long ldq,
+                             const double* K, long ldk,
+                             const double* V, long ldv,
+                             int causal, const int* kv_lengths,
+                             const int* rows, int n_rows,
+                             double* O, long ldo, double* P, int nthreads) {
+    return attention_impl(B, Tq, Tkv, h, h_kv, dk, dv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths,
+                          rows, n_rows, O, ldo, P, nthreads, 0);
 }
 
 /* Plain multi-head attention: every query head has its own K/V head. */
@@ -245,13 +281,13 @@ int oracle_attention(int B, int Tq, int Tkv, int h, int dk, int dv,
  *   if gated:  Gf = Xq W[:, G block] + b[G block];  Ocat *= 1 / (1 + exp(-Gf))
  *   Y  = Ocat Wo + bo  (+ R)
  */
-int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk, int dv,
-                          int gated, const double* Xq, const double* Xkv,
-                          const double* Wqkv, const double* bqkv,
-                          const double* Wo, const double* bo, const double* R,
-                          int causal, const int* kv_lengths,
-                          const int* rows, int n_rows,
-                          double* Y, int nthreads) {
+static int forward_impl(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk, int dv,
+                        int gated, const double* Xq, const double* Xkv,
+                        const double* Wqkv, const double* bqkv,
+                        const double* Wo, const double* bo, const double* R,
+                        int causal, const int* kv_lengths,
+                        const int* rows, int n_rows,
+                        double* Y, int nthreads, int rounded) {
     if (B < 0 || Tq < 0 || Tkv < 0 || D <= 0 || h <= 0 || dk <= 0 || dv <= 0) return ORACLE_BAD_ARG;
     if (h_kv <= 0 || h % h_kv != 0) return ORACLE_BAD_ARG;
     if (!Xq || !Wqkv || !Wo || !Y) return ORACLE_BAD_ARG;
@@ -293,6 +329,11 @@ int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk
     rc = oracle_linear((long)B * Tkv, D, hkv, Xkv, D, Wqkv + v_off, wcols, bqkv ? bqkv + v_off : NULL, Vf,
                        hkv, nthreads);
     if (rc) goto done;
+    if (rounded) {
+        round_all(Qf, (long)B * n_out * hq);
+        round_all(Kf, (long)B * Tkv * hk);
+        round_all(Vf, (long)B * Tkv * hkv);
+    }
     {
         /* the attention step sees the selected rows as a (B, n_out) query
            block; the causal test needs each row's original index t, so the
@@ -307,12 +348,12 @@ int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk
                 for (int r = 0; r < n_out; ++r)
                     memcpy(Qfull + ((long)b * Tq + rows[r]) * hq, Qf + ((long)b * n_out + r) * hq,
                            sizeof(double) * (size_t)hq);
-            rc = oracle_attention_grouped(B, Tq, Tkv, h, h_kv, dk, dv, Qfull, hq, Kf, hk, Vf, hkv, causal,
-                                          kv_lengths, rows, n_rows, Oc, hv, NULL, nthreads);
+            rc = attention_impl(B, Tq, Tkv, h, h_kv, dk, dv, Qfull, hq, Kf, hk, Vf, hkv, causal,
+                                kv_lengths, rows, n_rows, Oc, hv, NULL, nthreads, rounded);
             free(Qfull);
         } else {
-            rc = oracle_attention_grouped(B, Tq, Tkv, h, h_kv, dk, dv, Qf, hq, Kf, hk, Vf, hkv, causal,
-                                          kv_lengths, NULL, 0, Oc, hv, NULL, nthreads);
+            rc = attention_impl(B, Tq, Tkv, h, h_kv, dk, dv, Qf, hq, Kf, hk, Vf, hkv, causal,
+                                kv_lengths, NULL, 0, Oc, hv, NULL, nthreads, rounded);
         }
         if (rc) goto done;
     }
@@ -321,8 +362,10 @@ int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk
         rc = oracle_linear((long)B * n_out, D, hv, Xsel, D, Wqkv + g_off, wcols, bqkv ? bqkv + g_off : NULL,
                            Gf, hv, nthreads);
         if (rc) goto done;
+        if (rounded) round_all(Gf, (long)B * n_out * hv);
         for (long e = 0; e < (long)B * n_out * hv; ++e) Oc[e] = Oc[e] * (1.0 / (1.0 + exp(-Gf[e])));
     }
+    if (rounded) round_all(Oc, (long)B * n_out * hv);
     rc = oracle_linear((long)B * n_out, hv, D, Oc, hv, Wo, D, bo, Y, D, nthreads);
     if (rc) goto done;
     if (R) {
@@ -334,6 +377,7 @@ int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk
                 for (int c = 0; c < D; ++c) y[c] += rr[c];
             }
     }
+    if (rounded) round_all(Y, (long)B * n_out * D);
 done:
     free(Xsel);
     free(Qf);
@@ -342,6 +386,29 @@ done:
     free(Oc);
     free(Gf);
     return rc;
+}
+
+int oracle_mha_forward_ex(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk, int dv,
+                          int gated, const double* Xq, const double* Xkv,
+                          const double* Wqkv, const double* bqkv,
+                          const double* Wo, const double* bo, const double* R,
+                          int causal, const int* kv_lengths,
+                          const int* rows, int n_rows,
+                          double* Y, int nthreads) {
+    return forward_impl(B, Tq, Tkv, D, h, h_kv, dk, dv, gated, Xq, Xkv, Wqkv, bqkv, Wo, bo, R, causal,
+                        kv_lengths, rows, n_rows, Y, nthreads, 0);
+}
+
+/* The forward with bf16 rounding at the GPU path's storage points (see the header). */
+int oracle_mha_forward_rounded(int B, int Tq, int Tkv, int D, int h, int h_kv, int dk, int dv,
+                               int gated, const double* Xq, const double* Xkv,
+                               const double* Wqkv, const double* bqkv,
+                               const double* Wo, const double* bo, const double* R,
+                               int causal, const int* kv_lengths,
+                               const int* rows, int n_rows,
+                               double* Y, int nthreads) {
+    return forward_impl(B, Tq, Tkv, D, h, h_kv, dk, dv, gated, Xq, Xkv, Wqkv, bqkv, Wo, bo, R, causal,
+                        kv_lengths, rows, n_rows, Y, nthreads, 1);
 }
 
 /* The plain forward: h K/V heads, no gate, no residual. */

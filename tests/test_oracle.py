@@ -382,6 +382,72 @@ def test_bf16_rounding_matches_torch():
     assert np.array_equal(ours, ref)
 
 
+# ---------------------------------------------------------------- rounded diagnostic mode
+
+def test_oracle_bf16_rounding_ties_to_even_and_matches_torch(oracle_mod):
+    """The rounded mode's own bf16 rounding: ties go to the even neighbour, and on float32
+    inputs it agrees with torch's float32 -> bfloat16 conversion bit for bit."""
+    r = oracle_mod.round_bf16
+    assert r(1.0 + 2.0 ** -8) == 1.0                      # tie, 1.0 is even
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6      # tie, 1 + 2^-6 is even
+    assert r(-(1.0 + 2.0 ** -8 + 2.0 ** -20)) == -(1.0 + 2.0 ** -7)  # just above a tie
+    assert r(0.0) == 0.0 and r(2.0 ** -100) == 2.0 ** -100
+    torch = _torch()
+    rng = np.random.default_rng(23)
+    a = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ref = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([r(float(v)) for v in a])
+    assert np.array_equal(got, ref)
+
+
+def test_rounded_mode_rounds_the_weights_but_not_their_sum(oracle_mod):
+    """One query, two keys, d = 1, every projection exact: scores 1 and 1.5, so the
+    unnormalised weights are e^-0.5 and 1.  The rounded mode divides bf16(e^-0.5) * v_0 +
+    1 * v_1 by the unrounded sum e^-0.5 + 1 and rounds the result; the plain mode is the
+    textbook value."""
+    Xq = np.array([[[1.0]]])
+    Xkv = np.array([[[1.0], [1.5]]])
+    Wqkv = np.array([[1.0, 1.0, 1.0]])  # Q = x, K = x, V = x
+    Wo = np.array([[1.0]])
+    kw = dict(h=1, d_k=1, d_v=1, Xkv=Xkv)
+    p0 = math.exp(-0.5)
+    plain = oracle_mod.mha_forward(Xq, Wqkv, None, Wo, None, **kw)
+    rounded = oracle_mod.mha_forward(Xq, Wqkv, None, Wo, None, round_bf16=True, **kw)
+    assert plain[0, 0, 0] == pytest.approx((p0 * 1.0 + 1.5) / (p0 + 1.0), rel=1e-15)
+    p0_bf16 = float(wl.round_to_bf16(np.array([p0], dtype=np.float32))[0])
+    assert p0_bf16 != p0
+    o = (p0_bf16 * 1.0 + 1.5) / (p0 + 1.0)
+    o_bf16 = float(wl.round_to_bf16(np.array([o], dtype=np.float32))[0])
+    assert rounded[0, 0, 0] == o_bf16
+
+
+def test_rounded_mode_is_exact_when_nothing_needs_rounding(oracle_mod):
+    """Small integers everywhere and one key per query: every stored value is a bf16 number,
+    so the rounded mode equals the plain forward exactly."""
+    rng = np.random.default_rng(29)
+    Xq = rng.integers(-3, 4, (2, 1, 8)).astype(np.float64)
+    Wqkv = rng.integers(-1, 2, (8, 24)).astype(np.float64)
+    Wo = rng.integers(-1, 2, (8, 8)).astype(np.float64)
+    bq = rng.integers(-2, 3, 24).astype(np.float64)
+    plain = oracle_mod.mha_forward(Xq, Wqkv, bq, Wo, None, h=2, d_k=4, d_v=4)
+    rounded = oracle_mod.mha_forward(Xq, Wqkv, bq, Wo, None, h=2, d_k=4, d_v=4, round_bf16=True)
+    assert np.array_equal(plain, rounded)
+
+
+def test_rounded_mode_stays_within_the_bf16_budget(oracle_mod):
+    """On bf16 inputs the rounded forward differs from the plain one by about the bf16
+    storage error: more than nothing, well under the parity bound."""
+    w = wl.custom("rounded", B=2, T_q=70, D=128, h=2, d_k=64, causal=True)
+    x = wl.make_inputs(w, seed=4)
+    args = (x["X_q"], x["W_qkv"], x["b_qkv"], x["W_o"], x["b_o"], w.h, w.d_k, w.d_v)
+    plain = oracle_mod.mha_forward(*args, causal=True)
+    rounded = oracle_mod.mha_forward(*args, causal=True, round_bf16=True)
+    rel = np.linalg.norm(rounded - plain) / np.linalg.norm(plain)
+    assert 5e-4 < rel < 5e-3
+    # Y itself is bf16: every rounded output is a bf16 number
+    assert np.array_equal(rounded.astype(np.float32), wl.round_to_bf16(rounded.astype(np.float32)))
+
+
 def test_named_workloads_are_seeded_and_shaped():
     for name, w in wl.WORKLOADS.items():
         if w.B * w.T_q * w.D > 2_000_000:

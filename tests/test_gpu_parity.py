@@ -100,6 +100,31 @@ def test_linear_segments_writes_every_needed_row():
         assert_close(got[rows], ref[rows], "bf16", f"segment {i} (length {L})")
 
 
+def test_linear_segments_edge_cases():
+    """Every segment empty: no row block is needed, nothing is written (the kernel runs with
+    no tiles).  Lengths past the segment count as the whole segment; segments shorter than
+    one tile, and a row count that is not a multiple of 256, still give exact rows."""
+    layer = Mha(64, 1, 64, dtype=torch.bfloat16)
+    K, N = 128, 256
+    W = wl.random_tensor((K, N), seed=32, scale=0.05)
+    Wd = to_device(W, "bf16")
+    for seg, lens in ((300, [0, 0, 0]), (300, [0, 301, 5]), (100, [3, 100, 0, 77, 50]),
+                      (260, [260, 1, 130])):
+        lens = np.array(lens, dtype=np.int32)
+        A = wl.random_tensor((len(lens) * seg, K), seed=31)
+        C = torch.full((len(lens) * seg, N), 7.0, dtype=torch.bfloat16, device="cuda")
+        layer.linear_segments(to_device(A, "bf16"), Wd, None, torch.from_numpy(lens).cuda(), seg, out=C)
+        torch.cuda.synchronize()
+        got, ref = to_host(C), oracle.linear(A, W)
+        if not lens.any():
+            assert (got == 7.0).all()
+        for i, L in enumerate(lens):
+            need = min((min(max(int(L), 0), seg) + 127) // 128 * 128, seg)
+            rows = slice(i * seg, i * seg + need)
+            if need:
+                assert_close(got[rows], ref[rows], "bf16", f"segment {i} of {seg} (length {L})")
+
+
 def test_linear_strided_operands():
     """Row strides wider than the rows (a column block of W_qkv, as the
     cross-attention path uses)."""

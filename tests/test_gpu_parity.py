@@ -6,9 +6,7 @@ on the same seeded inputs.
     element, over shapes that span several tiles and a ragged tail;
   * the whole forward (mha_forward) on small shapes, element by element,
     including cross-attention with key padding, d = 64 and 128, fp32 and bf16;
-  * the five named workloads at full size: the fp32 ones element by element,
-    the bf16 ones on sampled query rows (tile edges, first and last rows) that
-    the oracle computes one by one;
+  * the five named workloads at full size, every output element;
   * edge cases: empty batch, one query row, one valid key, invalid lengths
     (NaN rows and a device status), guard bands around the output, padding
     invariance, determinism.
@@ -154,6 +152,13 @@ ATTN_CASES = [
     (2, 300, 300, 2, 64, True, [300, 129], 1.0),           # causal + padding
     (1, 384, 384, 2, 64, True, None, 4.0),                 # large scores: rescale path
     (2, 256, 520, 1, 128, False, [520, 257], 3.0),
+    # more work items (query tile x (batch, head)) than the d = 64 kernel's persistent grid of
+    # two CTAs per SM, so every CTA runs several items and starts item k+1 (its Q load, first K
+    # tiles and first score MMA) while item k drains
+    (8, 1024, 1024, 8, 64, True, None, 1.0),               # causal, 512 items
+    (4, 1024, 1024, 16, 64, False, None, 1.0),             # no mask, 512 items
+    (16, 384, 1000, 8, 64, False,                          # key lengths, batches sorted by
+     [int(v) for v in np.random.default_rng(5).integers(1, 1001, 16)], 1.0),  # length, 384 items
 ]
 
 
@@ -254,30 +259,20 @@ def test_named_f32_full(name):
     print(name, e)
 
 
-SAMPLED_ROWS = {
-    "c3_bf16_causal": [0, 1, 127, 128, 129, 1000, 2046, 2047],
-    "c4_bf16_causal_long": [0, 1, 127, 128, 8191, 16383],
-    "c5_bf16_cross": [0, 1, 127, 255, 511],
-}
-
-
-@pytest.mark.parametrize("name", list(SAMPLED_ROWS))
-def test_named_bf16_full_sampled_rows(name):
-    """The full-size workload through mha_forward (as the benchmark runs it);
-    the oracle computes the sampled query rows of every batch one by one."""
+@pytest.mark.parametrize("name", ["c3_bf16_causal", "c4_bf16_causal_long", "c5_bf16_cross"])
+def test_named_bf16_full(name):
+    """The full-size bf16 workloads through mha_forward (as the benchmark runs it), every
+    output element against the oracle.  c3 runs 1024 work items on the persistent d = 64
+    attention kernel (several per CTA), c5 768 with key lengths; c4 is one 16384-long causal
+    sequence at d = 128 (the oracle needs about a minute of host time for it)."""
     w = wl.WORKLOADS[name]
     x = wl.make_inputs(w)
     layer, y = _run_forward(w, x)
     assert layer.status() == _lib.MHA_OK
-    rows = SAMPLED_ROWS[name]
-    got = to_host(y[:, rows, :])
-    ref = _oracle_forward(w, x, rows=rows)
-    e = assert_close(got, ref, "bf16", name)
+    got = to_host(y)
+    del y
+    e = assert_close(got, _oracle_forward(w, x), "bf16", name)
     print(name, e)
-    # properties that hold at any size, over every row: finite, and not all equal
-    yy = y.float()
-    assert torch.isfinite(yy).all()
-    assert float(yy.std()) > 0
 
 
 # ------------------------------------------------------------------ edge cases

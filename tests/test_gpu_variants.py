@@ -214,8 +214,8 @@ def test_decode_long_cache_many_groups():
 def test_decode_ignores_cache_rows_past_the_length(d, h_kv):
     """Cache rows at or past L_b are not part of the step (itwiki.kr "멀티 헤드 어텐션",
     section 추론 비용과 변형: the cache holds the earlier tokens); they may hold anything, here
-    NaN, and the output must neither see them nor turn NaN (one row per cached head runs on
-    CUDA cores, grouped heads on the tensor core)."""
+    NaN, and the output must neither see them nor turn NaN (every case runs on the tensor-core
+    decode kernel, which zeroes those V rows before the PV product and masks those keys)."""
     h, Tq = 8, 1
     B, Tmax = 3, 700
     lengths = [Tmax, 130, 513]

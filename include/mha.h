@@ -355,23 +355,29 @@ const char* mha_strerror(mha_status status);
  *
  *  - Arguments, layouts and result are those of mha_forward.  The handle's own workspace
  *    (mha_set_workspace) is neither used nor modified.
+ *  - status_out: NULL, or a 4-byte aligned device int32 that receives this call's device
+ *    status (MHA_OK, MHA_ERR_TIMEOUT or MHA_ERR_BAD_LENGTH, as mha_get_status reports it for
+ *    mha_forward), copied on `stream` after the last kernel.  mha_get_status cannot see it:
+ *    it reads the handle's own workspace.
  *  - Returns MHA_ERR_WORKSPACE, before any CUDA call, when mha_workspace_size(B, T_q, T_kv)
- *    exceeds MHA_STATIC_WORKSPACE_BYTES.
+ *    exceeds MHA_STATIC_WORKSPACE_BYTES; every other argument error of mha_forward is also
+ *    reported before the array or *status_out is touched.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *    with that device current) and remembers it; make that first call before any stream
- *    capture.
+ *  - The first call on a device (and again after that device's context was destroyed and
+ *    created anew, as by cudaDeviceReset) looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and remembers it for that context;
+ *    make that first call before any stream capture.  Concurrent first calls from several
+ *    host threads are safe.
  *  - All calls share the one array, which keeps the previous call's contents: calls that
  *    overlap on the GPU (other streams or host threads on the same device) race on it and
  *    must be serialised by the caller.
- *  - Each call zeroes the status word first (cudaMemsetAsync on `stream`).  An L_b outside
- *    [1, T_kv] still gives NaN rows, but the status word cannot be read back: mha_get_status
- *    reads the handle's own workspace.
+ *  - Each call zeroes the array's status word first (cudaMemsetAsync on `stream`).
  */
 mha_status mha_forward_static_workspace(mha_t handle, const void* X_q, const void* X_kv, int B,
                                         int T_q, int T_kv, const void* W_qkv, const void* b_qkv,
                                         const void* W_o, const void* b_o, int causal,
-                                        const int32_t* kv_lengths, void* out, void* stream);
+                                        const int32_t* kv_lengths, void* out,
+                                        int32_t* status_out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -249,3 +249,28 @@ def test_forward_host_rejects_bad_arguments_before_any_copy(lib):
         assert fwd() == L.MHA_ERR_WORKSPACE                    # no workspace attached
     finally:
         L.mha_destroy(hdl)
+
+
+def test_static_workspace_rejects_bad_arguments_before_any_cuda_call(lib):
+    """mha_forward_static_workspace refuses every invalid call on the host, before it looks
+    up or touches its scratch array (so these run without a GPU)."""
+    bf = L.mha_create(1024, 16, 64, 64, L.MHA_BF16)
+    fake = 1 << 40                                   # never dereferenced: rejected earlier
+    try:
+        def fwd(**kw):
+            a = dict(X_q=fake, X_kv=None, B=1, T_q=128, T_kv=128, W_qkv=fake + (1 << 34),
+                     b_qkv=None, W_o=fake + (1 << 35), b_o=None, causal=1, kv_lengths=None,
+                     out=fake + (1 << 36), status_out=fake + (1 << 37), stream=None)
+            a.update(kw)
+            return L.mha_forward_static_workspace(bf, check=False, **a)
+        assert L.mha_forward_static_workspace(None, fake, None, 1, 128, 128, fake, None, fake,
+                                              None, 1, None, fake, None, None,
+                                              check=False) == L.MHA_ERR_INVALID_ARG
+        assert fwd(B=4, T_q=2048, T_kv=2048) == L.MHA_ERR_WORKSPACE  # 64 MiB > 32 MiB array
+        assert fwd(X_q=fake + 2) == L.MHA_ERR_INVALID_ARG             # bf16 alignment
+        assert fwd(out=fake) == L.MHA_ERR_INVALID_ARG                 # output aliases X_q
+        assert fwd(T_kv=64) == L.MHA_ERR_INVALID_ARG                  # self-attention, T_kv != T_q
+        assert fwd(status_out=fake + 2) == L.MHA_ERR_INVALID_ARG      # status word alignment
+        assert fwd(B=0) == L.MHA_OK                                   # empty batch: nothing to do
+    finally:
+        L.mha_destroy(bf)

@@ -53,7 +53,7 @@ _SIGNATURES = {
     "mha_decode": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp]),
     "mha_get_status": (_i, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "mha_forward_static_workspace": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp,
-                                          _vp, _vp]),
+                                          _vp, _vp, _vp]),
     "mha_check_wait_timeout": (_i, [_vp, _i64, _vp]),
     "mha_strerror": (ctypes.c_char_p, [_i]),
 }
@@ -223,9 +223,11 @@ MHA_STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 def mha_forward_static_workspace(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal,
-                                 kv_lengths, out, stream, check: bool = True) -> int:
+                                 kv_lengths, out, status_out, stream, check: bool = True) -> int:
     """mha_forward with the library's own fixed scratch array instead of a caller workspace
-    (for callers that may not allocate device memory; see include/mha.h)."""
+    (for callers that may not allocate device memory; see include/mha.h).  status_out: device
+    address of an int32 that receives the call's device status, or None."""
     code = load().mha_forward_static_workspace(handle, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv,
-                                               W_o, b_o, int(causal), kv_lengths, out, stream)
+                                               W_o, b_o, int(causal), kv_lengths, out, status_out,
+                                               stream)
     return _check("mha_forward_static_workspace", code) if check else code

@@ -27,6 +27,12 @@ struct mha_s {
 
 namespace mha {
 
+// Every host-side check of mha_forward_ex except the one on the attached workspace
+// (mha_api.cu).  MHA_OK: the call would launch its kernels, or nothing for B == 0 or T_q == 0.
+mha_status check_forward(const mha_s* m, const void* X_q, const void* X_kv, int B, int T_q,
+                         int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                         const void* b_o, int causal, const void* residual, const void* out);
+
 // Launch a kernel that may start while the previous kernel on the stream is finishing
 // (programmatic dependent launch): its CTAs run their set-up (barriers, TMEM allocation)
 // early and wait in grid_dependency_wait() until the previous grid has completed and its

@@ -407,15 +407,20 @@ mha_status mha_attention(mha_t handle, int B, int T_q, int T_kv, const void* Q, 
                             kv_lengths, O, ldo, stream);
 }
 
-mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
-                          const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
-                          int causal, const int32_t* kv_lengths, const void* residual, void* out,
-                          void* stream) {
-    if (handle == nullptr) return MHA_ERR_INVALID_ARG;
-    const mha_s* m = handle;
+}  // extern "C"
+
+namespace mha {
+
+// Every host-side check of mha_forward_ex except the workspace's: MHA_OK means the call
+// launches its kernels (or, for B == 0 or T_q == 0, nothing) once a large enough workspace
+// is attached.
+mha_status check_forward(const mha_s* m, const void* X_q, const void* X_kv, int B, int T_q,
+                         int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                         const void* b_o, int causal, const void* residual, const void* out) {
+    if (m == nullptr) return MHA_ERR_INVALID_ARG;
     const bool self = (X_kv == nullptr || X_kv == X_q);
     if (self && T_kv != T_q) return MHA_ERR_INVALID_ARG;
-    mha_status st = check_attention_shape(m, B, T_q, T_kv, causal);
+    const mha_status st = check_attention_shape(m, B, T_q, T_kv, causal);
     if (st != MHA_OK) return st;
     if (B == 0 || T_q == 0) return MHA_OK;
     if (T_kv == 0) return MHA_ERR_INVALID_ARG;
@@ -442,6 +447,28 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
     // the same element of Y is written: it may be Y itself, but not partly overlap it
     if (residual != nullptr && residual != out && overlaps(out, out_bytes, residual, out_bytes))
         return MHA_ERR_INVALID_ARG;
+    return MHA_OK;
+}
+
+}  // namespace mha
+
+extern "C" {
+
+mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q, int T_kv,
+                          const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                          int causal, const int32_t* kv_lengths, const void* residual, void* out,
+                          void* stream) {
+    const mha_s* m = handle;
+    mha_status st = mha::check_forward(m, X_q, X_kv, B, T_q, T_kv, W_qkv, b_qkv, W_o, b_o, causal,
+                                       residual, out);
+    if (st != MHA_OK) return st;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    const bool self = (X_kv == nullptr || X_kv == X_q);
+    const size_t s = elem_bytes(m->dtype);
+    const int64_t D = m->D;
+    const Widths wd = widths(m);
+    const int64_t hv = (int64_t)m->h * m->dv;
+    const int64_t ncols = wd.all();
     const WsLayout w = ws_layout(m, B, T_q, T_kv);
     if (m->ws == nullptr || m->ws_bytes < w.total) return MHA_ERR_WORKSPACE;
 

@@ -224,50 +224,36 @@ def cpu_baseline(w, budget_s: float = 15.0):
                       f"fp64, {dt:.2f} s"}
 
 
-def run_ours(args):
-    import torch
-    rank, world, local_rank = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-
-    import __graft_entry__ as g
-    g.build_library()
+def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
+    """Time workload w: K steps of mha_forward (each bracketed by events, L2 flushed before
+    it), then the same launches with events between them (per-kernel durations), then the
+    host-buffer forward through the C ABI.  Returns the figures of one JSON line."""
     from transformer_head_scaled_02_gb300 import Mha
-
-    w = wl.WORKLOADS[args.workload]
     x = wl.make_inputs(w)
     d = {k: to_device(v, w.dtype, torch) for k, v in x.items() if k != "kv_lengths"}
     kvl = None if x["kv_lengths"] is None else torch.from_numpy(x["kv_lengths"]).cuda()
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     layer = Mha(w.D, w.h, w.d_k, w.d_v, dtype=tdt)
     out = torch.empty((w.B, w.T_q, w.D), dtype=tdt, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    launches_per_step = 4 if w.cross else 3
 
     def forward():
         layer.forward(d["X_q"], d["W_qkv"], d["b_qkv"], d["W_o"], d["b_o"], X_kv=d["X_kv"],
                       causal=w.causal, kv_lengths=kvl, out=out)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         forward()
     torch.cuda.synchronize()
     if layer.status() != 0:
-        raise RuntimeError("device status not clean after warm-up")
+        raise RuntimeError(f"{w.name}: device status not clean after warm-up")
 
     # ---------------- timed region: K steps, each timed by events, L2 flushed between
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    sampler = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.05)
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.05)
     wall0 = time.perf_counter()
     for k in range(K):
         flush.zero_()
@@ -277,12 +263,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
-    sampler.stop()
+    if sampler is not None:
+        sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / K
     if layer.status() != 0:
-        raise RuntimeError("device status reports an error after the timed region")
+        raise RuntimeError(f"{w.name}: device status reports an error after the timed region")
 
     fl = wl.flops(w, x["kv_lengths"])
     # with key padding, only the valid keys count: the padded ones need neither projection nor
@@ -291,17 +278,16 @@ def run_ours(args):
     flops_counted = "algorithmic (valid keys only)" if "alg_total" in fl else "nominal"
     value = world * step_flops / (ms_per_step / 1e3) / 1e12
 
-    # ---------------- per-kernel durations: the same three launches, events between them
+    # ---------------- per-kernel durations: the same launches, events between them
     sf = wl.step_flops(w)
     names = ["qkv_proj", "attention", "out_proj"]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     Wqkv, bqkv = d["W_qkv"], d["b_qkv"]
     hq, hv = w.h * w.d_k, w.h * w.d_v
     ncols = 2 * hq + hv
-    qkv = torch.empty((w.B, w.T_q, ncols), dtype=tdt, device=dev)
     ocat = torch.empty((w.B, w.T_q, hv), dtype=tdt, device=dev)
-    per_kernel = None
     if not w.cross:
+        qkv = torch.empty((w.B, w.T_q, ncols), dtype=tdt, device=dev)
         X2 = d["X_q"].view(-1, w.D)
         for k in range(K):
             flush.zero_()
@@ -319,7 +305,7 @@ def run_ours(args):
                       for i, n in enumerate(names)}
     else:
         # cross-attention: the query projection, the key/value projection, attention, output
-        # projection; "qkv_proj" is the two projection launches together
+        # projection, each timed alone
         hk = w.h * w.d_k
         qb = torch.empty((w.B, w.T_q, hq), dtype=tdt, device=dev)
         kvb = torch.empty((w.B, w.T_kv, hk + hv), dtype=tdt, device=dev)
@@ -344,9 +330,8 @@ def run_ours(args):
             layer.linear(ocat.view(-1, hv), d["W_o"], d["b_o"], out=out.view(-1, w.D))
             e[4].record()
         torch.cuda.synchronize()
-        launch_ms = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
-                     for i, n in enumerate(["q_proj", "kv_proj", "attention", "out_proj"])}
-        per_kernel = launch_ms
+        per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
+                      for i, n in enumerate(["q_proj", "kv_proj", "attention", "out_proj"])}
         # FLOPs per launch; with key lengths the kernels visit only the L_b valid keys of each
         # batch (the key/value projection skips whole 256-row blocks past them)
         L = float(w.B * w.T_kv)
@@ -385,54 +370,101 @@ def run_ours(args):
     d2h = yh.numel() * yh.element_size()
 
     pk, pk_src = peaks()
-    roofline = None
-    if per_kernel:
-        top = max(per_kernel, key=per_kernel.get)
-        src = "attn_bf16.cu" if top == "attention" else "gemm_bf16.cu"
-        if w.dtype == "f32":
-            src = "simt_f32.cu"
-        ach = sf[top] / (per_kernel[top] / 1e3) / 1e12
-        if w.dtype == "f32":
-            # fp32 runs as FFMA on the CUDA cores: SMs x 128 fp32 lanes x 2 FLOP x max SM clock
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            mhz = float(pk.get("sm_max_mhz", 2070.0))
-            peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 1)
-            bound, peak_source = "alu", f"derived fp32 FFMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
-        else:
-            peak = pk["bf16_tflops"]
-            bound, peak_source = "tensor", f"{pk_src} bf16 dense (burst)"
-        roofline = {"kernel": top, "bound": bound, "achieved": round(ach, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                    "traffic": recorded_traffic(top, w.name, src),
-                    "peak_source": peak_source,
-                    "per_kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
-                    "per_kernel_frac_of_peak": {k: round(sf[k] / (v / 1e3) / 1e12 / peak, 4)
-                                                for k, v in per_kernel.items()}}
+    top = max(per_kernel, key=per_kernel.get)
+    src = "attn_bf16.cu" if top == "attention" else "gemm_bf16.cu"
+    if w.dtype == "f32":
+        src = "simt_f32.cu"
+    ach = sf[top] / (per_kernel[top] / 1e3) / 1e12
+    if w.dtype == "f32":
+        # fp32 runs as FFMA on the CUDA cores: SMs x 128 fp32 lanes x 2 FLOP x max SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = float(pk.get("sm_max_mhz", 2070.0))
+        peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 1)
+        bound, peak_source = "alu", f"derived fp32 FFMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
+    else:
+        peak = pk["bf16_tflops"]
+        bound, peak_source = "tensor", f"{pk_src} bf16 dense (burst)"
+    roofline = {"kernel": top, "bound": bound, "achieved": round(ach, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "traffic": recorded_traffic(top, w.name, src),
+                "peak_source": peak_source,
+                "per_kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
+                "per_kernel_frac_of_peak": {k: round(sf[k] / (v / 1e3) / 1e12 / peak, 4)
+                                            for k, v in per_kernel.items()}}
+    return {
+        "workload": w, "value": value, "ms_per_step": ms_per_step, "step_flops": step_flops,
+        "flops_counted": flops_counted, "nominal_flops": fl["total"], "roofline": roofline,
+        "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "chunks": e2e_chunks,
+                "note": "mha_forward_host through the C ABI: pinned host X in and Y out, the batch "
+                        "in chunks whose host-device copies overlap the kernels; weights resident"},
+        "launches_per_step": 4 if w.cross else 3, "wall": wall, "peak": pk["bf16_tflops"],
+        "peak_source": pk_src,
+    }
 
+
+# the other bf16 workloads, timed in the same process after the headline one and reported
+# under "other_workloads" of the same line
+EXTRA_WORKLOADS = ["c4_bf16_causal_long", "c5_bf16_cross"]
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__ as g
+    g.build_library()
+
+    w = wl.WORKLOADS[args.workload]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(torch.cuda.current_device())
+    r = measure_workload(w, args.steps, args.warmup, torch, dev, world, flush, sampler)
+    K = args.steps
+    pk = r["peak"]
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights; no dataset)",
         "config": {"workload": w.name, "B": w.B, "T_q": w.T_q, "T_kv": w.T_kv, "D": w.D,
                    "h": w.h, "d_k": w.d_k, "d_v": w.d_v, "causal": w.causal, "cross": w.cross,
-                   "flops_per_step": step_flops, "flops_counted": flops_counted,
-                   "nominal_flops_per_step": fl["total"],
-                   "frac_of_peak": round(value / world / pk["bf16_tflops"], 4),
-                   "peak_tflops": pk["bf16_tflops"], "peak_source": pk_src,
+                   "flops_per_step": r["step_flops"], "flops_counted": r["flops_counted"],
+                   "nominal_flops_per_step": r["nominal_flops"],
+                   "frac_of_peak": round(r["value"] / world / pk, 4),
+                   "peak_tflops": pk, "peak_source": r["peak_source"],
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline,
-        "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4),
-                "chunks": e2e_chunks,
-                "note": "mha_forward_host through the C ABI: pinned host X in and Y out, the batch "
-                        "in chunks whose host-device copies overlap the kernels; weights resident"},
-        "gpu_launches": launches_per_step * K,
+        "roofline": r["roofline"],
+        "e2e": r["e2e"],
+        "gpu_launches": r["launches_per_step"] * K,
         "clocks": sampler.summary(),
-        "wall_s_timed_region": round(wall, 3),
+        "wall_s_timed_region": round(r["wall"], 3),
     }
+    if world == 1 and not args.no_other_workloads:
+        others = {}
+        for name in EXTRA_WORKLOADS:
+            if name == w.name:
+                continue
+            ow = wl.WORKLOADS[name]
+            s2 = ClockSampler(torch.cuda.current_device())
+            o = measure_workload(ow, K, args.warmup, torch, dev, world, flush, s2)
+            others[name] = {
+                "value": round(o["value"], 2), "unit": UNIT, "ms_per_step": round(o["ms_per_step"], 4),
+                "frac_of_peak": round(o["value"] / pk, 4), "flops_per_step": o["step_flops"],
+                "flops_counted": o["flops_counted"], "nominal_flops_per_step": o["nominal_flops"],
+                "config": {"B": ow.B, "T_q": ow.T_q, "T_kv": ow.T_kv, "D": ow.D, "h": ow.h,
+                           "d_k": ow.d_k, "causal": ow.causal, "cross": ow.cross},
+                "roofline": o["roofline"], "e2e": o["e2e"], "clocks": s2.summary(),
+                "steps": K, "warmup": args.warmup}
+        line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_baseline_seconds)
     if rank == 0:
@@ -645,6 +677,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only --workload (by default c4 and c5 follow in the same run)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--variant", choices=sorted(VARIANTS), default=None,

@@ -13,6 +13,9 @@ latter halved under the causal mask, per batch element.
 One step = one mha_forward of the whole workload (three kernels: QKV GEMM,
 fused attention, output GEMM) on inputs already resident in HBM; L2 is flushed
 (a 256 MiB write) before every timed step, outside the events that time it.
+Before each timed loop the stream spins on the GPU long enough for the host to
+queue all K steps, so the events time the GPU's work rather than the host's
+launch latency.
 Under torchrun each rank runs an independent replica (the layer does not
 shard: there is no exchange step), the timed region is bracketed by a barrier
 and a device synchronise, and the slowest rank's time is reported.
@@ -40,6 +43,10 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "c3_bf16_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# GPU clock cycles the stream spins (torch.cuda._sleep) per queued step before a timed loop, so
+# that the host has queued every step's launches before the GPU reaches the first event: the
+# events then time the GPU work, not the gaps left while Python prepares the next launch
+PREQUEUE_CYCLES_PER_STEP = 200_000
 # batch chunks of the end-to-end (host buffers) measurement; each chunk's copies overlap the
 # other chunks' kernels
 E2E_CHUNKS = 2
@@ -255,6 +262,7 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
         sampler.start()
         time.sleep(0.05)
     wall0 = time.perf_counter()
+    torch.cuda._sleep(PREQUEUE_CYCLES_PER_STEP * K)
     for k in range(K):
         flush.zero_()
         ev[k][0].record()
@@ -286,6 +294,8 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
     hq, hv = w.h * w.d_k, w.h * w.d_v
     ncols = 2 * hq + hv
     ocat = torch.empty((w.B, w.T_q, hv), dtype=tdt, device=dev)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(PREQUEUE_CYCLES_PER_STEP * K)
     if not w.cross:
         qkv = torch.empty((w.B, w.T_q, ncols), dtype=tdt, device=dev)
         X2 = d["X_q"].view(-1, w.D)
@@ -359,6 +369,7 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
     for _ in range(2):
         forward_host()
     torch.cuda.synchronize()
+    torch.cuda._sleep(PREQUEUE_CYCLES_PER_STEP * Ke)
     for k in range(Ke):
         flush.zero_()
         eev[k][0].record()
@@ -497,6 +508,7 @@ def _timed_steps(torch, fn, flush, K, warmup):
         fn()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda._sleep(PREQUEUE_CYCLES_PER_STEP * K)
     for k in range(K):
         flush.zero_()
         ev[k][0].record()

@@ -72,6 +72,11 @@ static_assert(AttnCfg<128>::SMEM <= 232448, "smem budget d=128");
 
 constexpr int A_THREADS = 384;
 
+// K/V bytes of one group of (batch, head) pairs in the d = 128 kernel's CTA order
+#ifndef MHA_D128_GROUP_BYTES
+#define MHA_D128_GROUP_BYTES (64ll << 20)
+#endif
+
 // One row of a 128-key score tile from TMEM into registers (warp-collective), with the
 // causal / key-length mask applied (keys [0, lim) are visible).
 __device__ __forceinline__ void load_s_tile(uint32_t taddr, bool masked, int kv0, int lim,
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmO, int h, int h_kv, int T_q, int T_kv,
                         int causal, const int32_t* __restrict__ kv_lengths,
                         const __nv_bfloat16* __restrict__ gate, int64_t ldg, float scale_log2,
-                        int* status) {
+                        int* status, int BH, int n_qb, int head_group) {
     static_assert(HD == 128, "head dim 64 runs on attn_bf16_d64_kernel");
     using C = AttnCfg<HD>;
     constexpr int S = C::STAGES;
@@ -158,11 +163,20 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+    // CTA i of the 1-D grid (CTAs start roughly in index order): the (batch, head) pairs form
+    // groups of head_group; a group's CTAs come before the next group's, and within a group the
+    // query-tile pairs are numbered longest first (causal: the last pair of every (batch, head)
+    // first), the group's (batch, head) pairs fastest.  The CTAs in flight then read the K/V
+    // of about two groups, which stays in L2 while each of its query-tile pairs streams it.
+    const int gi = (int)blockIdx.x / (head_group * n_qb);
+    const int gr = (int)blockIdx.x - gi * head_group * n_qb;
+    const int gsz = min(head_group, BH - gi * head_group);
+    const int rank = gr / gsz;
+    const int bh = gi * head_group + (gr - rank * gsz);
     const int b = bh / h;
     const int head = bh - b * h;
     const int kvh = head / (h / h_kv);  // grouped K/V heads: the K/V head of this query head
-    const int qb = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+    const int qb = causal ? n_qb - 1 - rank : rank;
     const int q0 = qb * (C::NQ * C::BM);
 
     if (threadIdx.x == 0) {
@@ -1025,10 +1039,18 @@ cudaError_t launch_attn_hd(const void* Q, int64_t ldq, const void* K, int64_t ld
     if (err != cudaSuccess) return err;
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     const int rows_per_cta = C::NQ * C::BM;
-    const dim3 grid((unsigned)(B * h), (unsigned)((T_q + rows_per_cta - 1) / rows_per_cta));
-    return launch_pdl(kernel, grid, dim3(A_THREADS), C::SMEM, stream, tQ, tK, tV, tO,
+    const int BH = B * h;
+    const int n_qb = (T_q + rows_per_cta - 1) / rows_per_cta;
+    // (batch, head) pairs per group: the K/V of one group (4 T_kv d bytes per pair) within
+    // MHA_D128_GROUP_BYTES
+    const int64_t kv_head_bytes = 4 * (int64_t)T_kv * HD;
+    int64_t hg = (int64_t)MHA_D128_GROUP_BYTES / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+    hg = hg < 1 ? 1 : (hg > BH ? BH : hg);
+    const int64_t ctas = (int64_t)BH * n_qb;
+    if (ctas > INT32_MAX) return cudaErrorInvalidValue;
+    return launch_pdl(kernel, dim3((unsigned)ctas), dim3(A_THREADS), C::SMEM, stream, tQ, tK, tV, tO,
                       h, h_kv, T_q, T_kv, causal, kv_lengths, reinterpret_cast<const __nv_bfloat16*>(G),
-                      ldg, scale_log2, status);
+                      ldg, scale_log2, status, BH, n_qb, (int)hg);
 }
 
 }  // namespace

@@ -48,6 +48,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// One bf16 (x rounded to nearest even) to shared memory.
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&h))
+                 : "memory");
+}
+
 // Residual of one thread's row for the 64 columns of chunk c (zeros outside C).
 __device__ __forceinline__ void load_residual(const __nv_bfloat16* R, int64_t ldr, int row, int nc, int M,
                                               int N, uint4 (&dst)[8]) {
@@ -617,6 +624,259 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         tmem_dealloc_pair(tmem_base, G_TMEM_COLS);
     }
 }
+
+// ---------------------------------------------------------------------------------------
+// CTA-pair version with the accumulator transposed: tiles of 192 rows of A (the MMA's N
+// dimension) x 256 columns of W (the MMA's M dimension, 128 per CTA), for shapes where
+// 192-row tiles fill the pairs in less time than 256 x 256 ones (M = 8192, N = K = 768: 129
+// tiles in two rounds of smaller tiles against 96 in two full rounds).  The 192-row side comes
+// from A, whose K-major layout allows 96 rows per CTA; W, MN-major, could not be split into
+// 96-column halves in its 128-byte swizzled 64-column chunks.
+//   MMA A operand  W^T: each CTA's 128 columns of W, MN-major (W's rows are K), 128-byte
+//                  swizzled 64-column chunks, exactly as the other kernel stages its half of B;
+//   MMA B operand  A^T: 96 rows of A per CTA, K-major, 128-byte swizzle (a 96-row half of a
+//                  192-row tile is twelve 8-row groups, which a K-major operand allows);
+//   accumulator    TMEM lane = output column n (the CTA's 128), TMEM column = output row m
+//                  (all 192 of the tile, from both CTAs' halves of A).
+// Epilogue: each thread holds one output column across the tile's rows; it adds that column's
+// bias, rounds, and writes 64-row x 32-column boxes (row-major, no swizzle: the 32 lanes of a
+// warp write one 64-byte row segment per store) that a TMA store sends to C.
+constexpr int T_BM = 192;                          // rows of A per tile (96 per CTA)
+constexpr int T_HALF_X = 96 * 64 * 2;              // 12 KB: 96 rows x 64 K of A
+constexpr int T_X_BYTES = 2 * T_HALF_X;            // 24 KB per stage
+constexpr int T_W_CHUNK = 64 * 64 * 2;             // 8 KB: 64 K-rows x 64 columns of W
+constexpr int T_HALF_W = 2 * T_W_CHUNK;            // 16 KB: 64 K-rows x this CTA's 128 columns
+constexpr int T_W_BYTES = 2 * T_HALF_W;            // 32 KB per stage
+constexpr int T_STAGES = 3;
+constexpr int T_EPI_BUF = 64 * 32 * 2;             // 4 KB: 64 rows x 32 columns
+constexpr int T_EPI_BYTES = 4 * 2 * T_EPI_BUF;
+constexpr int T_SMEM = T_STAGES * (T_X_BYTES + T_W_BYTES) + T_EPI_BYTES + G_BAR_BYTES + 1024;
+static_assert(T_SMEM <= 232448, "shared memory budget (transposed pair)");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
+    gemm_bf16_pairT_kernel(const __grid_constant__ CUtensorMap tmX,
+                           const __grid_constant__ CUtensorMap tmW,
+                           const __grid_constant__ CUtensorMap tmC,
+                           const __nv_bfloat16* __restrict__ bias, int M, int N, int K, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sX = base;
+    const uint32_t sW = sX + T_STAGES * T_X_BYTES;
+    const uint32_t sE = sW + T_STAGES * T_W_BYTES;
+    const uint32_t sBar = sE + T_EPI_BYTES;
+    // barrier layout (same offsets in both CTAs): full[S], empty[S], tfull[2], tempty[2], drain
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8u * T_STAGES;
+    const uint32_t bar_tfull = sBar + 16u * T_STAGES;
+    const uint32_t bar_tempty = bar_tfull + 16u;
+    const uint32_t bar_drain = bar_tempty + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = (int)(blockIdx.x >> 1);
+    const int npairs = (int)(gridDim.x >> 1);
+    const int num_m = (M + T_BM - 1) / T_BM;
+    const int num_n = (N + G_BN - 1) / G_BN;
+    const int num_tiles = num_m * num_n;
+    const int num_k = (K + P_BK - 1) / P_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T_STAGES; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8u * a, 1);
+            mbar_init(bar_tempty + 8u * a, 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), G_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // inputs may come from the previous kernel on the stream
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs): own 96 rows of A, own 128 columns of W
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+                const int m0 = (tile / num_n) * T_BM + (int)rank * 96;
+                const int nb = (tile % num_n) * G_BN + (int)rank * 128;
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(bar_full + 8u * stage, 0);
+                    const int halves = kb * P_BK + 64 < K ? 2 : 1;
+                    if (leader)
+                        mbar_arrive_expect_tx(bar_full + 8u * stage, 2 * halves * (T_HALF_X + T_HALF_W));
+                    for (int hh = 0; hh < halves; ++hh) {
+                        const int k0 = kb * P_BK + hh * 64;
+                        tma_load_2d_pair(sX + stage * T_X_BYTES + hh * T_HALF_X, &tmX, k0, m0, fb);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d_pair(sW + stage * T_W_BYTES + hh * T_HALF_W + c * T_W_CHUNK, &tmW,
+                                             nb + c * 64, k0, fb);
+                    }
+                    ++issued;
+                    if (++stage == T_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (leader)
+                for (int back = 0; back < T_STAGES && back < issued; ++back) {
+                    stage = stage == 0 ? T_STAGES - 1 : stage - 1;
+                    if (stage == T_STAGES - 1) phase ^= 1u;
+                    drain_wait(bar_full + 8u * stage, phase);
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (even CTA only): D (256 columns of W x 192 rows of A)
+            const uint32_t idesc = idesc_bf16_f32(256, T_BM, true, false);
+            const uint64_t wdesc0 = sdesc_sw128(sW, T_W_CHUNK, 1024);
+            const uint64_t xdesc0 = sdesc_sw128(sX, 16, 1024);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = pair; tile < num_tiles && ok; tile += npairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(bar_tempty + 8u * acc, acc_phase ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * T_BM);
+                for (int kb = 0; kb < num_k; ++kb) {
+                    if (!mbar_wait(bar_full + 8u * stage, phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t wd = wdesc0 + (uint64_t)((stage * T_W_BYTES) >> 4);
+                    const uint64_t xd = xdesc0 + (uint64_t)((stage * T_X_BYTES) >> 4);
+                    const int ksteps = kb * P_BK + 64 < K ? P_BK / 16 : 64 / 16;
+                    for (int k = 0; k < ksteps; ++k)
+                        mma_bf16_ss_pair(d_tmem, wd + (uint64_t)(((k >> 2) * T_HALF_W + (k & 3) * 2048) >> 4),
+                                         xd + (uint64_t)(((k >> 2) * T_HALF_X + (k & 3) * 32) >> 4), idesc,
+                                         (kb | k) != 0 ? 1u : 0u);
+                    tc_commit_pair_mc(bar_empty + 8u * stage, 0x3);
+                    if (++stage == T_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(bar_tfull + 8u * acc, 0x3);
+            }
+            tc_commit_pair_mc(bar_drain, 0x1);
+            drain_wait(bar_drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: this CTA's 128 output columns, one per thread
+        const int q = warp & 3;
+        const int e = warp - 2;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t buf0 = sE + (uint32_t)(e * 2 * T_EPI_BUF);
+        uint32_t bufsel = 0;
+        int it = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
+            const int m0 = (tile / num_n) * T_BM;
+            const int nw = (tile % num_n) * G_BN + (int)rank * 128 + q * 32;  // this warp's columns
+            const int n = nw + lane;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            const float bv = bias != nullptr && n < N ? __bfloat162float(bias[n]) : 0.f;
+            // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
+                break;
+            tc_fence_after();
+            const uint32_t t0 = tmem_base + lane_off + (uint32_t)(acc * T_BM);
+#pragma unroll 1
+            for (int ch = 0; ch < T_BM / 64; ++ch) {
+                uint32_t va[32], vb[32];
+                tmem_ld32(t0 + ch * 64, va);
+                tmem_ld32(t0 + ch * 64 + 32, vb);
+                tmem_wait_ld();
+                reg_fence(va);
+                reg_fence(vb);
+                if (ch == T_BM / 64 - 1) {
+                    // accumulator read: release it to the MMA issuer in the even CTA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(bar_tempty + 8u * acc);
+                        else
+                            mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * acc, 0));
+                    }
+                }
+                const int mr = m0 + ch * 64;
+                if (mr < M && nw < N) {  // else the box lies wholly outside C
+                    const uint32_t buf = buf0 + bufsel * (uint32_t)T_EPI_BUF;
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
+                    __syncwarp();
+                    // row i of the box: this lane's column at byte 2 * lane of a 64-byte row
+                    const uint32_t col = buf + 2u * (uint32_t)lane;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        st_shared_b16(col + (uint32_t)i * 64u, __uint_as_float(va[i]) + bv);
+                        st_shared_b16(col + (uint32_t)(i + 32) * 64u, __uint_as_float(vb[i]) + bv);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, nw, mr);
+                        bulk_commit_group();
+                    }
+                    bufsel ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // lanes that skipped a one-thread role wait here for it: the CTA barrier below must
+    // see whole warps, or it can complete while a role is still running
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the pair's MMAs may touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, G_TMEM_COLS);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
@@ -645,6 +905,63 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
     const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
     auto pair_kernel = R != nullptr ? gemm_bf16_pair_kernel<true> : gemm_bf16_pair_kernel<false>;
     auto tc_kernel = R != nullptr ? gemm_bf16_tc_kernel<true> : gemm_bf16_tc_kernel<false>;
+    if (M > 128 && R == nullptr && seg_len == nullptr) {
+        // 192-row tiles with the accumulator transposed, where they fill the pairs in less time
+        // than 256 x 256 ones: rounds of tiles over the resident pairs, a 192-row tile taking
+        // 0.91 of a 256-row one (measured: c3's QKV projection, 7 rounds of 192-row tiles
+        // against 6 of 256-row ones, 41.1 against 38.8 us; M = 8192, N = K = 768, 2 rounds
+        // each, 15.1 against 16.9 us)
+        static int t_pairs_cache[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int t_pairs = dev >= 0 && dev < 64 ? t_pairs_cache[dev] : 0;
+        if (t_pairs == 0) {
+            if (cudaFuncSetAttribute(gemm_bf16_pairT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     T_SMEM) != cudaSuccess)
+                return cudaErrorInvalidValue;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
+            cfg.blockDim = dim3(G_THREADS);
+            cfg.dynamicSmemBytes = T_SMEM;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_pairT_kernel, &cfg) != cudaSuccess || n <= 0)
+                n = num_sms / 2;
+            t_pairs = n;
+            if (dev >= 0 && dev < 64) t_pairs_cache[dev] = n;
+        }
+        const int64_t nb = (N + G_BN - 1) / G_BN;
+        const int64_t tiles_t = ((M + T_BM - 1) / T_BM) * nb, tiles_s = ((M + 255) / 256) * nb;
+        const int64_t cost_t = 91 * ((tiles_t + t_pairs - 1) / t_pairs);
+        const int64_t cost_s = 100 * ((tiles_s + t_pairs - 1) / t_pairs);
+        if (cost_t < cost_s) {
+            CUtensorMap tX, tCT;
+            {
+                const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+                const uint64_t strides[1] = {(uint64_t)lda * 2};
+                const uint32_t box[2] = {64, 96};
+                if (!encode_tmap_bf16(&tX, A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+            }
+            {
+                const uint64_t dims[2] = {(uint64_t)N, (uint64_t)M};
+                const uint64_t strides[1] = {(uint64_t)ldc * 2};
+                const uint32_t box[2] = {32, 64};
+                if (!encode_tmap_bf16(&tCT, C, 2, dims, strides, box, 0)) return cudaErrorInvalidValue;
+            }
+            cudaError_t err = cudaFuncSetAttribute(gemm_bf16_pairT_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+            if (err != cudaSuccess) return err;
+            const int pairs = tiles_t < t_pairs ? (int)tiles_t : t_pairs;
+            return launch_pdl(gemm_bf16_pairT_kernel, dim3(2 * pairs), dim3(G_THREADS), T_SMEM, stream, tX, tW,
+                              tCT, reinterpret_cast<const __nv_bfloat16*>(bias), M, N, K, status);
+        }
+    }
     if (M > 128) {
         // CTA pairs: the W box is 64 columns x 64 K-rows, the A box 64 K x 128 rows (as
         // above); each CTA of a pair loads its own A rows and its half of the W tile.

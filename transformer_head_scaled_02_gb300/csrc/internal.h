@@ -54,11 +54,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Encode a bf16 tiled tensor map with 128-byte swizzle and zero fill out of bounds.
-// dims[0] is the innermost (contiguous) extent; strides_bytes has rank-1 entries.
-// Returns false if the driver entry point is unavailable or rejects the map.
+// Encode a bf16 tiled tensor map with 128-byte swizzle (swizzle_bytes == 0: none) and zero
+// fill out of bounds.  dims[0] is the innermost (contiguous) extent; strides_bytes has rank-1
+// entries.  Returns false if the driver entry point is unavailable or rejects the map.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box);
+                      const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes = 128);
 
 // C = A W + bias (+ R), fp32 everywhere.  A (M,K) lda; W (K,N) ldw; R (M,N) ldr or null;
 // C (M,N) ldc.

@@ -46,8 +46,9 @@ static bool get_encoder() {
 }
 
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box) {
+                      const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes) {
     if (!get_encoder()) return false;
+    if (swizzle_bytes != 128 && swizzle_bytes != 0) return false;
     cuuint64_t gdim[5];
     cuuint64_t gstr[4];
     cuuint32_t bdim[5];
@@ -60,7 +61,8 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
     }
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                                 const_cast<void*>(base), gdim, gstr, bdim, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -20,20 +20,23 @@ namespace {
 
 constexpr int F_BN = 64;
 
-// BM x 64 output tile per block of BM * 4 threads, 4x4 outputs per thread (rows 4 ty..,
-// columns 4 tx..), K consumed in slices of BK.  Shared-memory tiles are double-buffered: the
-// next slice is loaded from global memory into registers while the current one is
-// multiplied, then stored to the other buffer, one barrier per slice.  A is staged
-// transposed (As[k][m]) so that both operands of a product step are one 16-byte shared load
-// each.  The K loop runs in order (k = 0, 1, ...) with one FFMA per product.  VEC: A and W
-// 16-byte aligned with row strides a multiple of 4 floats, so that four consecutive elements
-// of a row are one 16-byte global load.
-template <int BM, int BK, bool VEC>
-__global__ void __launch_bounds__(BM * 4)
+// 64 x 64 output tile per block of 128 threads, 8 x 4 outputs per thread (rows 8 ty..,
+// columns 4 tx..), K consumed in slices of BK.  Per k step a thread reads 8 A and 4 W values
+// (three 16-byte shared loads) for 32 multiply-adds, issued as 16 packed `fma.rn.f32x2`
+// (two IEEE fp32 fmas each: row pairs of A times a broadcast W value), so the FMA pipe, not
+// instruction issue, sets the pace.  Shared-memory tiles are double-buffered: the next slice
+// is loaded from global memory into registers while the current one is multiplied, then
+// stored to the other buffer, one barrier per slice.  A is staged transposed (As[k][m]) so
+// that both operands of a product step are 16-byte shared loads.  The K loop runs in order
+// (k = 0, 1, ...) with one fma per product.  VEC: A and W 16-byte aligned with row strides a
+// multiple of 4 floats, so that four consecutive elements of a row are one 16-byte global
+// load.
+template <int BK, bool VEC>
+__global__ void __launch_bounds__(128)
     gemm_f32_kernel(const float* __restrict__ A, int64_t lda, const float* __restrict__ W,
                     int64_t ldw, const float* __restrict__ bias, const float* R, int64_t ldr,
                     float* C, int64_t ldc, int M, int N, int K) {
-    constexpr int THREADS = BM * 4;
+    constexpr int BM = 64, THREADS = 128;
     constexpr int NA = BM * BK / 4 / THREADS;  // 4-element pieces of A per thread and slice
     constexpr int NW = BK * F_BN / 4 / THREADS;
     static_assert(NA >= 1 && NW >= 1, "slice smaller than the block");
@@ -89,9 +92,9 @@ __global__ void __launch_bounds__(BM * 4)
         }
     };
 
-    float acc[4][4];
+    float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     load(0);
@@ -103,22 +106,28 @@ __global__ void __launch_bounds__(BM * 4)
         if (more) load(k0 + BK);  // in flight while this slice is multiplied
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8 + 4]);
             const float4 b4 = *reinterpret_cast<const float4*>(&Ws[buf][kk][tx * 4]);
-            const float a[4] = {a4.x, a4.y, a4.z, a4.w};
-            const float b[4] = {b4.x, b4.y, b4.z, b4.w};
+            // rows (2p, 2p + 1) of the thread's eight, each W value in both halves
+            const uint64_t ap[4] = {pack2(a0.x, a0.y), pack2(a0.z, a0.w), pack2(a1.x, a1.y),
+                                    pack2(a1.z, a1.w)};
+            const uint64_t bp[4] = {pack2(b4.x, b4.x), pack2(b4.y, b4.y), pack2(b4.z, b4.z),
+                                    pack2(b4.w, b4.w)};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int p = 0; p < 4; ++p)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j)
+                    unpack2(fma2(ap[p], bp[j], pack2(acc[2 * p][j], acc[2 * p + 1][j])), acc[2 * p][j],
+                            acc[2 * p + 1][j]);
         }
         if (more) store(buf ^ 1);  // the other buffer was last read before the previous barrier
         __syncthreads();
         buf ^= 1;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int gm = m0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + ty * 8 + i;
         if (gm >= M) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -128,20 +137,6 @@ __global__ void __launch_bounds__(BM * 4)
                     acc[i][j] + (bias ? bias[gn] : 0.f) + (R ? R[(int64_t)gm * ldr + gn] : 0.f);
         }
     }
-}
-
-template <int BM, int BK>
-cudaError_t launch_gemm_f32_cfg(const float* A, int64_t lda, const float* W, int64_t ldw,
-                                const float* bias, const float* R, int64_t ldr, float* C,
-                                int64_t ldc, int M, int N, int K, cudaStream_t stream) {
-    const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + BM - 1) / BM));
-    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0) &&
-                     lda % 4 == 0 && ldw % 4 == 0;
-    if (vec)
-        gemm_f32_kernel<BM, BK, true><<<grid, BM * 4, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
-    else
-        gemm_f32_kernel<BM, BK, false><<<grid, BM * 4, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
-    return cudaGetLastError();
 }
 
 constexpr int FA_BQ = 16;      // query rows per block (4 per warp)
@@ -484,9 +479,16 @@ cudaError_t launch_attn_f32_tiled(const float* Q, int64_t ldq, const float* K, i
 cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t ldw,
                             const float* bias, const float* R, int64_t ldr, float* C, int64_t ldc,
                             int M, int N, int K, cudaStream_t stream) {
-    // 64-row tiles, 32-wide K slices: measured best of 64/32/16 rows x 16/32 K on the
-    // 1024 x 512 x {1536, 512} projections of the fp32 causal workload
-    return launch_gemm_f32_cfg<64, 32>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, stream);
+    // 32-wide K slices: 16-wide ones measured slower on the 1024 x 512 x {1536, 512}
+    // projections of the fp32 causal workload (43.7 / 28.4 against 42.4 / 20.3 us)
+    const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + 63) / 64));
+    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0) &&
+                     lda % 4 == 0 && ldw % 4 == 0;
+    if (vec)
+        gemm_f32_kernel<32, true><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+    else
+        gemm_f32_kernel<32, false><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attn_f32(const float* Q, int64_t ldq, const float* K, int64_t ldk,

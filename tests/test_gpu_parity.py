@@ -76,6 +76,19 @@ def test_linear_step(dtype, M, K, N, bias):
     assert_close(to_host(C), oracle.linear(A, W, b), dtype, f"linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(70, 37, 45), (129, 130, 67), (64, 33, 64)])
+def test_linear_step_f32_unaligned(M, K, N):
+    """fp32 projections whose row strides are not a multiple of four floats take the scalar
+    global loads of the fp32 GEMM (no 16-byte loads); the sums are the same."""
+    A = wl.random_tensor((M, K), seed=4, dtype="f32")
+    W = wl.random_tensor((K, N), seed=5, dtype="f32", scale=0.05)
+    b = wl.random_tensor((N,), seed=6, dtype="f32", scale=0.1)
+    layer = Mha(64, 1, 64, dtype=torch.float32)
+    C = layer.linear(to_device(A, "f32"), to_device(W, "f32"), to_device(b, "f32"))
+    torch.cuda.synchronize()
+    assert_close(to_host(C), oracle.linear(A, W, b), "f32", f"f32 linear {M}x{K}x{N}")
+
+
 def test_linear_segments_writes_every_needed_row():
     """mha_linear_segments: the rows of each segment below its length rounded up to 128 equal
     the oracle's projection (the rest may be skipped).  Segments of 700 rows straddle the

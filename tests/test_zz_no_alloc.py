@@ -83,7 +83,9 @@ def test_static_workspace_matches_oracle_and_mha_forward_twice(w):
             torch.cuda.synchronize()
         # the second call allocated nothing on the device
         assert torch.cuda.mem_get_info()[0] == free_before
+        # the static calls' device status, copied out to the caller's words
         assert status.tolist() == [_lib.MHA_OK, _lib.MHA_OK]
+        # the handle's own workspace holds only the ordinary call's status
         assert _lib.mha_get_status(handle, stream) == _lib.MHA_OK
         r = to_host(ref)
         o = _oracle(w, x)

@@ -314,41 +314,38 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
         per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
                       for i, n in enumerate(names)}
     else:
-        # cross-attention: the query projection, the key/value projection, attention, output
-        # projection, each timed alone
+        # cross-attention: the key/value and query projections in one launch (as the forward
+        # runs them, rows past the key lengths not projected), attention, output projection,
+        # each timed alone
         hk = w.h * w.d_k
         qb = torch.empty((w.B, w.T_q, hq), dtype=tdt, device=dev)
         kvb = torch.empty((w.B, w.T_kv, hk + hv), dtype=tdt, device=dev)
         Xq2, Xkv2 = d["X_q"].view(-1, w.D), d["X_kv"].view(-1, w.D)
         bq = None if bqkv is None else bqkv[:hq]
         bkv = None if bqkv is None else bqkv[hq:]
-        kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
         for k in range(K):
             flush.zero_()
             e = kev[k]
             e[0].record()
-            layer.linear(Xq2, Wqkv[:, :hq], bq, out=qb.view(-1, hq))
+            layer.linear_pair(Xkv2, Wqkv[:, hq:], bkv, Xq2, Wqkv[:, :hq], bq, seg_len=kvl,
+                              seg_rows=w.T_kv if kvl is not None else 0,
+                              out=kvb.view(-1, hk + hv), out2=qb.view(-1, hq))
             e[1].record()
-            if kvl is None:
-                layer.linear(Xkv2, Wqkv[:, hq:], bkv, out=kvb.view(-1, hk + hv))
-            else:  # as the forward runs it: rows past the key lengths are not projected
-                layer.linear_segments(Xkv2, Wqkv[:, hq:], bkv, kvl, w.T_kv, out=kvb.view(-1, hk + hv))
-            e[2].record()
             layer.attention(qb, kvb[..., :hk], kvb[..., hk:], causal=w.causal, kv_lengths=kvl,
                             out=ocat)
-            e[3].record()
+            e[2].record()
             layer.linear(ocat.view(-1, hv), d["W_o"], d["b_o"], out=out.view(-1, w.D))
-            e[4].record()
+            e[3].record()
         torch.cuda.synchronize()
         per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(K))
-                      for i, n in enumerate(["q_proj", "kv_proj", "attention", "out_proj"])}
+                      for i, n in enumerate(["kv_q_proj", "attention", "out_proj"])}
         # FLOPs per launch; with key lengths the kernels visit only the L_b valid keys of each
         # batch (the key/value projection skips whole 256-row blocks past them)
         L = float(w.B * w.T_kv)
         if x["kv_lengths"] is not None:
             import numpy as np
             L = float(np.sum(np.asarray(x["kv_lengths"], dtype=np.float64)))
-        sf = dict(sf, q_proj=2.0 * w.D * w.B * w.T_q * hq, kv_proj=2.0 * w.D * L * (hk + hv),
+        sf = dict(sf, kv_q_proj=2.0 * w.D * w.B * w.T_q * hq + 2.0 * w.D * L * (hk + hv),
                   attention=2.0 * w.h * w.T_q * L * (w.d_k + w.d_v) * (0.5 if w.causal else 1.0))
 
     # ---------------- end to end through the public API, host buffers in and out

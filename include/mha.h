@@ -249,6 +249,25 @@ mha_status mha_linear_ex(mha_t handle, const void* A, int64_t lda, int M, int K,
  * seg_len NULL, seg_rows <= 0 or M not a multiple of seg_rows: MHA_ERR_INVALID_ARG; other
  * arguments as for mha_linear.
  */
+/*
+ * mha_linear_pair -- two independent projections that share the inner dimension K, in one
+ * launch where possible: C = A W + bias (M x N; with seg_len, the rows of each segment past
+ * its length may be left unwritten exactly as in mha_linear_segments) and C2 = A2 W2 + bias2
+ * (M2 x N2).  Cross-attention projects its key/value side and its query side this way
+ * (itwiki.kr "멀티 헤드 어텐션", tensor-shape table row 투영, with the query and key/value inputs
+ * of the cross-attention form): for bf16 handles with M > 128 and M2 > 128 both run on one
+ * persistent grid of CTA pairs, so the smaller one fills the larger one's last round instead of
+ * adding rounds of its own; otherwise they run one after the other on `stream`.
+ * Arguments as for mha_linear (both) and mha_linear_segments (seg_len, seg_rows; seg_len may be
+ * NULL, then seg_rows is ignored).  M2 == 0 or M == 0 skips that projection.  C and C2 may not
+ * overlap each other or any input of either projection (MHA_ERR_INVALID_ARG).
+ */
+mha_status mha_linear_pair(mha_t handle, const void* A, int64_t lda, int M, const void* W,
+                           int64_t ldw, int N, const void* bias, const int32_t* seg_len,
+                           int seg_rows, void* C, int64_t ldc, const void* A2, int64_t lda2,
+                           int M2, const void* W2, int64_t ldw2, int N2, const void* bias2,
+                           void* C2, int64_t ldc2, int K, void* stream);
+
 mha_status mha_linear_segments(mha_t handle, const void* A, int64_t lda, int M, int K,
                                const void* W, int64_t ldw, int N, const void* bias,
                                const int32_t* seg_len, int seg_rows, void* C, int64_t ldc,

@@ -185,6 +185,26 @@ def test_decode_and_linear_ex_reject_bad_arguments(lib):
         assert seg(ldc=32) == L.MHA_ERR_INVALID_ARG                 # as mha_linear: C row < N
         assert seg(A=fake + 2) == L.MHA_ERR_INVALID_ARG             # misaligned bf16 pointer
         assert seg(M=0) == L.MHA_OK
+
+        def pair(**kw):
+            a = dict(A=fake, lda=64, M=512, W=fake + (1 << 28), ldw=64, N=64, bias=None, lens=None,
+                     seg_rows=0, C=fake + (3 << 28), ldc=64, A2=fake + (4 << 28), lda2=64, M2=300,
+                     W2=fake + (5 << 28), ldw2=32, N2=32, bias2=None, C2=fake + (6 << 28), ldc2=32,
+                     K=64)
+            a.update(kw)
+            return L.mha_linear_pair(bf, a["A"], a["lda"], a["M"], a["W"], a["ldw"], a["N"], a["bias"],
+                                     a["lens"], a["seg_rows"], a["C"], a["ldc"], a["A2"], a["lda2"],
+                                     a["M2"], a["W2"], a["ldw2"], a["N2"], a["bias2"], a["C2"],
+                                     a["ldc2"], a["K"], None, check=False)
+        assert pair(lens=fake + (7 << 28), seg_rows=0) == L.MHA_ERR_INVALID_ARG
+        assert pair(lens=fake + (7 << 28), seg_rows=300) == L.MHA_ERR_INVALID_ARG  # M % 300
+        assert pair(ldc2=16) == L.MHA_ERR_INVALID_ARG           # second output row < N2
+        assert pair(A2=fake + (4 << 28) + 2) == L.MHA_ERR_INVALID_ARG  # misaligned bf16 pointer
+        assert pair(C2=fake + (3 << 28) + 64) == L.MHA_ERR_INVALID_ARG  # outputs overlap
+        assert pair(C2=fake + 128) == L.MHA_ERR_INVALID_ARG     # C2 over the first's A
+        assert pair(C=fake + (5 << 28)) == L.MHA_ERR_INVALID_ARG  # C over the second's W
+        assert pair(K=0) == L.MHA_ERR_INVALID_ARG
+        assert pair(M=0, M2=0) == L.MHA_OK
     finally:
         L.mha_destroy(bf)
         L.mha_destroy(odd)

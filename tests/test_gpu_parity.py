@@ -89,6 +89,40 @@ def test_linear_step_f32_unaligned(M, K, N):
     assert_close(to_host(C), oracle.linear(A, W, b), "f32", f"f32 linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("dtype,M,M2,N,N2,K,lens", [
+    ("bf16", 4 * 700, 300, 384, 200, 192, [1, 300, 700, 129]),   # one launch, segments, ragged
+    ("bf16", 1000, 8192, 1536, 768, 256, None),                  # one launch, second one larger
+    ("bf16", 600, 100, 256, 512, 128, None),                     # M2 <= 128: two launches
+    ("f32", 4 * 700, 300, 72, 40, 48, [1, 300, 700, 129]),       # fp32: two launches
+])
+def test_linear_pair(dtype, M, M2, N, N2, K, lens):
+    """mha_linear_pair: both outputs equal the oracle's projections (with segment lengths, the
+    rows the attention step reads), whether the two run in one launch or one after the other."""
+    A = wl.random_tensor((M, K), seed=31, dtype=dtype)
+    W = wl.random_tensor((K, N), seed=32, dtype=dtype, scale=0.05)
+    b = wl.random_tensor((N,), seed=33, dtype=dtype, scale=0.1)
+    A2 = wl.random_tensor((M2, K), seed=34, dtype=dtype)
+    W2 = wl.random_tensor((K, N2), seed=35, dtype=dtype, scale=0.05)
+    b2 = wl.random_tensor((N2,), seed=36, dtype=dtype, scale=0.1)
+    layer = Mha(64, 1, 64, dtype=torch_dtype(dtype))
+    seg = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.full((M, N), float("nan"), dtype=torch_dtype(dtype), device="cuda")
+    out2 = torch.full((M2, N2), float("nan"), dtype=torch_dtype(dtype), device="cuda")
+    layer.linear_pair(to_device(A, dtype), to_device(W, dtype), to_device(b, dtype),
+                      to_device(A2, dtype), to_device(W2, dtype), to_device(b2, dtype),
+                      seg_len=seg, seg_rows=0 if lens is None else 700, out=out, out2=out2)
+    torch.cuda.synchronize()
+    assert_close(to_host(out2), oracle.linear(A2, W2, b2), dtype, "second projection")
+    ref, got = oracle.linear(A, W, b), to_host(out)
+    if lens is None:
+        assert_close(got, ref, dtype, "first projection")
+    else:
+        for i, L in enumerate(lens):
+            need = min((int(L) + 127) // 128 * 128, 700)
+            rows = slice(i * 700, i * 700 + need)
+            assert_close(got[rows], ref[rows], dtype, f"first projection, segment {i} (length {L})")
+
+
 def test_linear_segments_writes_every_needed_row():
     """mha_linear_segments: the rows of each segment below its length rounded up to 128 equal
     the oracle's projection (the rest may be skipped).  Segments of 700 rows straddle the

@@ -45,6 +45,8 @@ _SIGNATURES = {
     "mha_linear": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp]),
     "mha_linear_ex": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i64, _vp, _i64, _vp]),
     "mha_linear_segments": (_i, [_vp, _vp, _i64, _i, _i, _vp, _i64, _i, _vp, _vp, _i, _vp, _i64, _vp]),
+    "mha_linear_pair": (_i, [_vp, _vp, _i64, _i, _vp, _i64, _i, _vp, _vp, _i, _vp, _i64,
+                             _vp, _i64, _i, _vp, _i64, _i, _vp, _vp, _i64, _i, _vp]),
     "mha_attention": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp, _vp, _i64,
                            _vp]),
     "mha_attention_ex": (_i, [_vp, _i, _i, _i, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i, _vp,
@@ -181,6 +183,12 @@ def mha_linear_segments(handle, A, lda, M, K, W, ldw, N, bias, seg_len, seg_rows
     code = load().mha_linear_segments(handle, A, lda, M, K, W, ldw, N, bias, seg_len, seg_rows, C,
                                       ldc, stream)
     return _check("mha_linear_segments", code) if check else code
+
+def mha_linear_pair(handle, A, lda, M, W, ldw, N, bias, seg_len, seg_rows, C, ldc, A2, lda2, M2, W2,
+                    ldw2, N2, bias2, C2, ldc2, K, stream, check: bool = True):
+    code = load().mha_linear_pair(handle, A, lda, M, W, ldw, N, bias, seg_len, seg_rows, C, ldc, A2,
+                                  lda2, M2, W2, ldw2, N2, bias2, C2, ldc2, K, stream)
+    return _check("mha_linear_pair", code) if check else code
 
 def mha_attention(handle, B, T_q, T_kv, Q, ldq, K, ldk, V, ldv, causal, kv_lengths, O, ldo,
                   stream, check: bool = True) -> int:

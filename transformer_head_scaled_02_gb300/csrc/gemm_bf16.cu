@@ -384,14 +384,21 @@ constexpr int P_SMEM = P_STAGES * P_STAGE_BYTES + G_EPI_BYTES + G_BAR_BYTES + P_
 
 static_assert(P_SMEM <= 232448, "shared memory budget (pair)");
 
-template <bool RESID>
+// TWO: a second, independent projection with the same K (tmA2 / tmW2 / tmC2, bias2, M2 x N2)
+// runs in the same launch, its tiles numbered after the first's: the cross-attention query
+// projection next to the key / value one, whose rounds it would otherwise add to the step.
+template <bool RESID, bool TWO>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmC,
                           const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* R,
                           int64_t ldr, int M, int N, int K, int* status,
-                          const int32_t* __restrict__ seg_len, int seg_rows) {
+                          const int32_t* __restrict__ seg_len, int seg_rows,
+                          const __grid_constant__ CUtensorMap tmA2,
+                          const __grid_constant__ CUtensorMap tmW2,
+                          const __grid_constant__ CUtensorMap tmC2,
+                          const __nv_bfloat16* __restrict__ bias2, int M2, int N2) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -439,6 +446,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmC);
+        if constexpr (TWO) {
+            tma_prefetch_desc(&tmA2);
+            tma_prefetch_desc(&tmW2);
+            tma_prefetch_desc(&tmC2);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), G_TMEM_COLS);
@@ -483,9 +495,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         __syncthreads();
         num_m = *mcount;
     }
-    const int num_tiles = num_m * num_n;
-    // tile -> first row of its 256-row block (N fastest: see above)
-    auto tile_row0 = [&](int tile) { return (listed ? (int)mlist[tile / num_n] : tile / num_n) * 256; };
+    const int tiles1 = num_m * num_n;
+    const int num_n2 = TWO ? (N2 + G_BN - 1) / G_BN : 1;
+    const int num_tiles = TWO ? tiles1 + ((M2 + 255) / 256) * num_n2 : tiles1;
+    // tile -> problem, first row of its 256-row block and first column (N fastest: see above)
+    auto decode = [&](int tile, int& prob, int& row0, int& n0) {
+        if (!TWO || tile < tiles1) {
+            prob = 0;
+            row0 = (listed ? (int)mlist[tile / num_n] : tile / num_n) * 256;
+            n0 = (tile % num_n) * G_BN;
+        } else {
+            const int t = tile - tiles1;
+            prob = 1;
+            row0 = (t / num_n2) * 256;
+            n0 = (t % num_n2) * G_BN;
+        }
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -495,8 +520,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-                const int m0 = tile_row0(tile) + (int)rank * 128;
-                const int nb = (tile % num_n) * G_BN + (int)rank * 128;
+                int prob, row0, n0;
+                decode(tile, prob, row0, n0);
+                const CUtensorMap* mA = TWO && prob ? &tmA2 : &tmA;
+                const CUtensorMap* mW = TWO && prob ? &tmW2 : &tmW;
+                const int m0 = row0 + (int)rank * 128;
+                const int nb = n0 + (int)rank * 128;
                 for (int kb = 0; kb < num_k; ++kb) {
                     if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) {
                         ok = false;
@@ -508,10 +537,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                         mbar_arrive_expect_tx(bar_full + 8u * stage, 2 * halves * (P_HALF_A + P_HALF_B));
                     for (int hh = 0; hh < halves; ++hh) {
                         const int k0 = kb * P_BK + hh * 64;
-                        tma_load_2d_pair(sA + stage * P_A_BYTES + hh * P_HALF_A, &tmA, k0, m0, fb);
+                        tma_load_2d_pair(sA + stage * P_A_BYTES + hh * P_HALF_A, mA, k0, m0, fb);
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
-                            tma_load_2d_pair(sB + stage * P_B_BYTES + hh * P_HALF_B + c * P_B_CHUNK, &tmW,
+                            tma_load_2d_pair(sB + stage * P_B_BYTES + hh * P_HALF_B + c * P_B_CHUNK, mW,
                                              nb + c * 64, k0, fb);
                     }
                     ++issued;
@@ -583,21 +612,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         uint32_t bufsel = 0;
         int it = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
-            const int m0 = tile_row0(tile) + (int)rank * 128;
-            const int n0 = (tile % num_n) * G_BN;
+            int prob, row0, n0;
+            decode(tile, prob, row0, n0);
+            const int m0 = row0 + (int)rank * 128;
+            const bool p2 = TWO && prob;
+            const __nv_bfloat16* tb = p2 ? bias2 : bias;
+            const int tM = p2 ? M2 : M, tN = p2 ? N2 : N;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // bias and the first 64 residual columns are fetched while the tile's MMAs run
-            const uint4 bvec = load_bias_lanes(bias, n0, N, lane);
+            const uint4 bvec = load_bias_lanes(tb, n0, tN, lane);
             uint4 res[RESID ? 8 : 1];
             if constexpr (RESID) load_residual(R, ldr, m0 + q * 32 + lane, n0, M, N, res);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * acc, acc_phase, abort_flag, status)))
                 break;
             tc_fence_after();
-            epilogue_rows<RESID>(tmem_base + lane_off + (uint32_t)(acc * G_BN), bvec, bias != nullptr,
-                                 m0 + q * 32, n0, lane, sE + (uint32_t)(e * 2 * G_EPI_BUF), bufsel, &tmC, R,
-                                 ldr, M, N, res, [&] {
+            epilogue_rows<RESID>(tmem_base + lane_off + (uint32_t)(acc * G_BN), bvec, tb != nullptr,
+                                 m0 + q * 32, n0, lane, sE + (uint32_t)(e * 2 * G_EPI_BUF), bufsel,
+                                 p2 ? &tmC2 : &tmC, R, ldr, tM, tN, res, [&] {
                                      // accumulator read: release it to the MMA issuer in the even CTA
                                      tc_fence_before();
                                      __syncwarp();
@@ -877,33 +910,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     }
 }
 
+// Co-resident clusters of a pair kernel (cached per kernel variant and device): the persistent
+// grid's size.
+template <typename Kernel>
+int pair_occupancy(Kernel kernel, int variant, int num_sms) {
+    static int cache[3][64] = {{0}};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int n = dev >= 0 && dev < 64 ? cache[variant][dev] : 0;
+    if (n > 0) return n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = P_SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+    if (dev >= 0 && dev < 64) cache[variant][dev] = n;
+    return n;
+}
+
+// The three tensor maps of one pair-kernel projection: A (K-major, 64 x 128 boxes), W (64 x 64
+// boxes of its (in, out) rows) and C (64 x 32 store boxes).
+bool encode_pair_maps(const void* A, int64_t lda, const void* W, int64_t ldw, void* C, int64_t ldc,
+                      int M, int N, int K, CUtensorMap* tA, CUtensorMap* tW, CUtensorMap* tC) {
+    const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)lda * 2};
+    const uint32_t ba[2] = {64, G_BM};
+    const uint64_t dw[2] = {(uint64_t)N, (uint64_t)K}, sw[1] = {(uint64_t)ldw * 2};
+    const uint32_t bw[2] = {64, G_BK};
+    const uint64_t dc[2] = {(uint64_t)N, (uint64_t)M}, sc[1] = {(uint64_t)ldc * 2};
+    const uint32_t bc[2] = {64, 32};
+    return encode_tmap_bf16(tA, A, 2, da, sa, ba) && encode_tmap_bf16(tW, W, 2, dw, sw, bw) &&
+           encode_tmap_bf16(tC, C, 2, dc, sc, bc);
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_bf16_two(const void* A, int64_t lda, const void* W, int64_t ldw,
+                                 const void* bias, void* C, int64_t ldc, int M, int N,
+                                 const int32_t* seg_len, int seg_rows, const void* A2, int64_t lda2,
+                                 const void* W2, int64_t ldw2, const void* bias2, void* C2,
+                                 int64_t ldc2, int M2, int N2, int K, int num_sms, int* status,
+                                 cudaStream_t stream) {
+    if (M <= 128 || M2 <= 128) return cudaErrorInvalidValue;
+    CUtensorMap tA, tW, tC, tA2, tW2, tC2;
+    if (!encode_pair_maps(A, lda, W, ldw, C, ldc, M, N, K, &tA, &tW, &tC) ||
+        !encode_pair_maps(A2, lda2, W2, ldw2, C2, ldc2, M2, N2, K, &tA2, &tW2, &tC2))
+        return cudaErrorInvalidValue;
+    auto kernel = gemm_bf16_pair_kernel<false, true>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    if (err != cudaSuccess) return err;
+    const int max_pairs = pair_occupancy(kernel, 2, num_sms);
+    const int64_t tiles = (int64_t)((M + 255) / 256) * ((N + G_BN - 1) / G_BN) +
+                          (int64_t)((M2 + 255) / 256) * ((N2 + G_BN - 1) / G_BN);
+    const int pairs = tiles < max_pairs ? (int)tiles : max_pairs;
+    const bool listed = seg_len != nullptr && seg_rows >= 128 && (M + 255) / 256 <= P_MLIST_MAX;
+    return launch_pdl(kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream, tA, tW, tC,
+                      reinterpret_cast<const __nv_bfloat16*>(bias),
+                      static_cast<const __nv_bfloat16*>(nullptr), (int64_t)0, M, N, K, status,
+                      listed ? seg_len : nullptr, listed ? seg_rows : 0, tA2, tW2, tC2,
+                      reinterpret_cast<const __nv_bfloat16*>(bias2), M2, N2);
+}
 
 cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t ldw,
                              const void* bias, const void* R, int64_t ldr, void* C, int64_t ldc,
                              int M, int N, int K, int num_sms, int* status, cudaStream_t stream,
                              const int32_t* seg_len, int seg_rows) {
     CUtensorMap tA, tW, tC;
-    {
-        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
-        const uint64_t strides[1] = {(uint64_t)lda * 2};
-        const uint32_t box[2] = {64, G_BM};
-        if (!encode_tmap_bf16(&tA, A, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)N, (uint64_t)K};
-        const uint64_t strides[1] = {(uint64_t)ldw * 2};
-        const uint32_t box[2] = {64, G_BK};
-        if (!encode_tmap_bf16(&tW, W, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)N, (uint64_t)M};
-        const uint64_t strides[1] = {(uint64_t)ldc * 2};
-        const uint32_t box[2] = {64, 32};
-        if (!encode_tmap_bf16(&tC, C, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
+    if (!encode_pair_maps(A, lda, W, ldw, C, ldc, M, N, K, &tA, &tW, &tC)) return cudaErrorInvalidValue;
     const int num_tiles = ((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
-    auto pair_kernel = R != nullptr ? gemm_bf16_pair_kernel<true> : gemm_bf16_pair_kernel<false>;
+    auto pair_kernel = R != nullptr ? gemm_bf16_pair_kernel<true, false> : gemm_bf16_pair_kernel<false, false>;
     auto tc_kernel = R != nullptr ? gemm_bf16_tc_kernel<true> : gemm_bf16_tc_kernel<false>;
     if (M > 128 && R == nullptr && seg_len == nullptr) {
         // 192-row tiles with the accumulator transposed, where they fill the pairs in less time
@@ -968,28 +1049,7 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         cudaError_t err = cudaFuncSetAttribute(pair_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
         if (err != cudaSuccess) return err;
-        static int max_pairs_cache[2][64] = {{0}};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int max_pairs = dev >= 0 && dev < 64 ? max_pairs_cache[R != nullptr][dev] : 0;
-        if (max_pairs == 0) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
-            cfg.blockDim = dim3(G_THREADS);
-            cfg.dynamicSmemBytes = P_SMEM;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = 2;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, pair_kernel, &cfg) != cudaSuccess || n <= 0)
-                n = num_sms / 2;
-            max_pairs = n;
-            if (dev >= 0 && dev < 64) max_pairs_cache[R != nullptr][dev] = n;
-        }
+        const int max_pairs = pair_occupancy(pair_kernel, R != nullptr ? 1 : 0, num_sms);
         const int pair_tiles = ((M + 255) / 256) * ((N + G_BN - 1) / G_BN);
         const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
         // the row-block list fits up to P_MLIST_MAX blocks; beyond that every row is computed
@@ -997,7 +1057,8 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         return launch_pdl(pair_kernel, dim3(2 * pairs), dim3(G_THREADS), P_SMEM, stream,
                           tA, tW, tC, reinterpret_cast<const __nv_bfloat16*>(bias),
                           reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status,
-                          listed ? seg_len : nullptr, listed ? seg_rows : 0);
+                          listed ? seg_len : nullptr, listed ? seg_rows : 0, tA, tW, tC,
+                          static_cast<const __nv_bfloat16*>(nullptr), 0, 0);
     }
     cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);

@@ -84,6 +84,16 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
                              int M, int N, int K, int num_sms, int* status, cudaStream_t stream,
                              const int32_t* seg_len = nullptr, int seg_rows = 0);
 
+// Two independent bf16 projections with the same K in one launch of the CTA-pair kernel
+// (both M > 128; no residual): C = A W + bias, rows past the segment lengths optionally
+// skipped as above, and C2 = A2 W2 + bias2.  cudaErrorInvalidValue if either M <= 128.
+cudaError_t launch_gemm_bf16_two(const void* A, int64_t lda, const void* W, int64_t ldw,
+                                 const void* bias, void* C, int64_t ldc, int M, int N,
+                                 const int32_t* seg_len, int seg_rows, const void* A2, int64_t lda2,
+                                 const void* W2, int64_t ldw2, const void* bias2, void* C2,
+                                 int64_t ldc2, int M2, int N2, int K, int num_sms, int* status,
+                                 cudaStream_t stream);
+
 // Fused flash attention on tcgen05 for head dim 64 or 128 (d_k == d_v), grouped K/V heads
 // (h_kv divides h) and an optional gate G.  num_sms sizes the persistent grid of the d = 64
 // kernel.

@@ -167,6 +167,31 @@ mha_status run_linear(const mha_s* m, const void* A, int64_t lda, int M, int K, 
     return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+// Two independent projections with the same K (validated): one launch for bf16 with both
+// M > 128, else one after the other.  seg_len / seg_rows apply to the first.
+mha_status run_linear_pair(const mha_s* m, const void* A, int64_t lda, int M, const void* W, int64_t ldw,
+                           int N, const void* bias, const int32_t* seg_len, int seg_rows, void* C,
+                           int64_t ldc, const void* A2, int64_t lda2, int M2, const void* W2,
+                           int64_t ldw2, int N2, const void* bias2, void* C2, int64_t ldc2, int K,
+                           cudaStream_t stream) {
+    if (m->dtype == MHA_BF16 && M > 128 && M2 > 128) {
+        int sms = 0;
+        const mha_status st = query_sms(&sms);
+        if (st != MHA_OK) return st;
+        const cudaError_t err =
+            mha::launch_gemm_bf16_two(A, lda, W, ldw, bias, C, ldc, M, N, seg_len, seg_rows, A2, lda2, W2,
+                                      ldw2, bias2, C2, ldc2, M2, N2, K, sms, status_ptr(m), stream);
+        return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+    }
+    if (M > 0) {
+        const mha_status st = run_linear(m, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc, stream,
+                                         seg_len, seg_len ? seg_rows : 0);
+        if (st != MHA_OK) return st;
+    }
+    if (M2 > 0) return run_linear(m, A2, lda2, M2, K, W2, ldw2, N2, bias2, nullptr, 0, C2, ldc2, stream);
+    return MHA_OK;
+}
+
 mha_status run_attention(const mha_s* m, int B, int T_q, int T_kv, const void* Q, int64_t ldq,
                          const void* K, int64_t ldk, const void* V, int64_t ldv, const void* G,
                          int64_t ldg, int causal, const int32_t* kv_lengths, void* O, int64_t ldo,
@@ -375,6 +400,31 @@ mha_status mha_linear_segments(mha_t handle, const void* A, int64_t lda, int M, 
                       static_cast<cudaStream_t>(stream), seg_len, seg_rows);
 }
 
+mha_status mha_linear_pair(mha_t handle, const void* A, int64_t lda, int M, const void* W,
+                           int64_t ldw, int N, const void* bias, const int32_t* seg_len,
+                           int seg_rows, void* C, int64_t ldc, const void* A2, int64_t lda2,
+                           int M2, const void* W2, int64_t ldw2, int N2, const void* bias2,
+                           void* C2, int64_t ldc2, int K, void* stream) {
+    if (seg_len != nullptr && (seg_rows <= 0 || M % seg_rows != 0)) return MHA_ERR_INVALID_ARG;
+    mha_status st = check_linear(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc);
+    if (st != MHA_OK) return st;
+    st = check_linear(handle, A2, lda2, M2, K, W2, ldw2, N2, bias2, nullptr, 0, C2, ldc2);
+    if (st != MHA_OK) return st;
+    if (M > 0 && M2 > 0) {
+        // neither output may overlap the other or the other projection's inputs
+        const size_t s = elem_bytes(handle->dtype);
+        const size_t c1 = ((size_t)(M - 1) * ldc + N) * s, c2 = ((size_t)(M2 - 1) * ldc2 + N2) * s;
+        if (overlaps(C, c1, C2, c2) || overlaps(C, c1, A2, ((size_t)(M2 - 1) * lda2 + K) * s) ||
+            overlaps(C, c1, W2, ((size_t)(K - 1) * ldw2 + N2) * s) ||
+            overlaps(C2, c2, A, ((size_t)(M - 1) * lda + K) * s) ||
+            overlaps(C2, c2, W, ((size_t)(K - 1) * ldw + N) * s))
+            return MHA_ERR_INVALID_ARG;
+    }
+    if (M == 0 && M2 == 0) return MHA_OK;
+    return run_linear_pair(handle, A, lda, M, W, ldw, N, bias, seg_len, seg_rows, C, ldc, A2, lda2, M2, W2,
+                           ldw2, N2, bias2, C2, ldc2, K, static_cast<cudaStream_t>(stream));
+}
+
 mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K, const void* W,
                       int64_t ldw, int N, const void* bias, void* C, int64_t ldc, void* stream) {
     return mha_linear_ex(handle, A, lda, M, K, W, ldw, N, bias, nullptr, 0, C, ldc, stream);
@@ -496,19 +546,18 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
         const int64_t qg = wd.q + wd.g;
         uint8_t* q = ws + w.q_off;
         uint8_t* kv = ws + w.kv_off;
-        st = run_linear(m, X_q, D, B * T_q, (int)D, W_qkv, ncols, (int)wd.q, b_qkv, nullptr, 0, q, qg, cs);
+        // key/value rows past each batch's key length (in whole 128-key tiles) are never read
+        // by the attention step, so their projection may be skipped
+        // (the query side [Q] next to them in the same launch; the gate block separately)
+        st = run_linear_pair(m, X_kv, D, B * T_kv, wqkv + k_off * s, ncols, (int)(wd.k + wd.v),
+                             bqkv ? bqkv + k_off * s : nullptr, kv_lengths, T_kv, kv, wd.k + wd.v, X_q, D,
+                             B * T_q, W_qkv, ncols, (int)wd.q, b_qkv, q, qg, (int)D, cs);
         if (st != MHA_OK) return st;
         if (m->gated) {
             st = run_linear(m, X_q, D, B * T_q, (int)D, wqkv + g_off * s, ncols, (int)wd.g,
                             bqkv ? bqkv + g_off * s : nullptr, nullptr, 0, q + wd.q * s, qg, cs);
             if (st != MHA_OK) return st;
         }
-        // key/value rows past each batch's key length (in whole 128-key tiles) are never read
-        // by the attention step, so their projection may be skipped
-        st = run_linear(m, X_kv, D, B * T_kv, (int)D, wqkv + k_off * s, ncols, (int)(wd.k + wd.v),
-                        bqkv ? bqkv + k_off * s : nullptr, nullptr, 0, kv, wd.k + wd.v, cs, kv_lengths,
-                        T_kv);
-        if (st != MHA_OK) return st;
         st = run_attention(m, B, T_q, T_kv, q, qg, kv, wd.k + wd.v, kv + wd.k * s, wd.k + wd.v,
                            m->gated ? q + wd.q * s : nullptr, qg, causal, kv_lengths, ocat, hv, cs);
         if (st != MHA_OK) return st;

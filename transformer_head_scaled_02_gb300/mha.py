@@ -191,6 +191,36 @@ class Mha:
                                  _stream())
         return out
 
+    def linear_pair(self, A: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor],
+                    A2: torch.Tensor, W2: torch.Tensor, bias2: Optional[torch.Tensor],
+                    seg_len: Optional[torch.Tensor] = None, seg_rows: int = 0,
+                    out: Optional[torch.Tensor] = None,
+                    out2: Optional[torch.Tensor] = None):
+        """(A W + bias, A2 W2 + bias2) in one launch where possible (the cross-attention key /
+        value and query projections); with seg_len, rows of the first past each segment's
+        length may be left unwritten as in linear_segments.  Returns (out, out2)."""
+        M, K = A.shape
+        M2, K2 = A2.shape
+        N, N2 = W.shape[1], W2.shape[1]
+        if K2 != K or W.shape[0] != K or W2.shape[0] != K:
+            raise ValueError("both projections need the same inner dimension")
+        if out is None:
+            out = torch.empty((M, N), dtype=self.dtype, device=A.device)
+        if out2 is None:
+            out2 = torch.empty((M2, N2), dtype=self.dtype, device=A.device)
+        for name, t in (("A", A), ("W", W), ("out", out), ("A2", A2), ("W2", W2), ("out2", out2)):
+            if not t.is_cuda or t.dtype != self.dtype or t.stride(1) != 1:
+                raise ValueError(f"{name} must be a row-major {self.dtype} CUDA matrix")
+        self._check("bias", bias, None if bias is None else (N,))
+        self._check("bias2", bias2, None if bias2 is None else (N2,))
+        if seg_len is not None and (seg_len.dtype != torch.int32 or not seg_len.is_cuda):
+            raise ValueError("seg_len must be a CUDA int32 tensor")
+        _lib.mha_linear_pair(self.handle, _ptr(A), A.stride(0), M, _ptr(W), W.stride(0), N, _ptr(bias),
+                             _ptr(seg_len), seg_rows, _ptr(out), out.stride(0), _ptr(A2), A2.stride(0),
+                             M2, _ptr(W2), W2.stride(0), N2, _ptr(bias2), _ptr(out2), out2.stride(0), K,
+                             _stream())
+        return out, out2
+
     def attention(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, causal: bool = False,
                   kv_lengths: Optional[torch.Tensor] = None,
                   out: Optional[torch.Tensor] = None,

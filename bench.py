@@ -407,9 +407,28 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
                 "ms_per_step": round(e2e_ms, 4), "chunks": e2e_chunks,
                 "note": "mha_forward_host through the C ABI: pinned host X in and Y out, the batch "
                         "in chunks whose host-device copies overlap the kernels; weights resident"},
-        "launches_per_step": 4 if w.cross else 3, "wall": wall, "peak": pk["bf16_tflops"],
+        "launches_per_step": launches_per_step(w), "wall": wall, "peak": pk["bf16_tflops"],
+        "step_ms": step_stats(step_ms),
         "peak_source": pk_src,
     }
+
+
+def launches_per_step(w) -> int:
+    """Kernels one forward launches: projections (self-attention: one; cross-attention: the
+    key/value and query projections in one launch for bf16 when both have more than 128 rows,
+    else two; a gate block one more), attention, output projection."""
+    if not w.cross:
+        return 3
+    paired = w.dtype == "bf16" and w.B * w.T_q > 128 and w.B * w.T_kv > 128
+    return (1 if paired else 2) + (1 if getattr(w, "gated", False) else 0) + 2
+
+
+def step_stats(step_ms) -> dict:
+    """Median and p10 / p90 of the timed steps (this rank's), in ms."""
+    import numpy as np
+    a = np.asarray(step_ms, dtype=np.float64)
+    return {"p10": round(float(np.percentile(a, 10)), 4), "median": round(float(np.median(a)), 4),
+            "p90": round(float(np.percentile(a, 90)), 4)}
 
 
 # the other bf16 workloads, timed in the same process after the headline one and reported
@@ -453,6 +472,7 @@ def run_ours(args):
         "roofline": r["roofline"],
         "e2e": r["e2e"],
         "gpu_launches": r["launches_per_step"] * K,
+        "step_ms": r["step_ms"],
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(r["wall"], 3),
     }
@@ -470,8 +490,8 @@ def run_ours(args):
                 "flops_counted": o["flops_counted"], "nominal_flops_per_step": o["nominal_flops"],
                 "config": {"B": ow.B, "T_q": ow.T_q, "T_kv": ow.T_kv, "D": ow.D, "h": ow.h,
                            "d_k": ow.d_k, "causal": ow.causal, "cross": ow.cross},
-                "roofline": o["roofline"], "e2e": o["e2e"], "clocks": s2.summary(),
-                "steps": K, "warmup": args.warmup}
+                "roofline": o["roofline"], "e2e": o["e2e"], "step_ms": o["step_ms"],
+                "clocks": s2.summary(), "steps": K, "warmup": args.warmup}
         line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_baseline_seconds)

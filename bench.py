@@ -48,8 +48,8 @@ L2_FLUSH_BYTES = 256 << 20
 # events then time the GPU work, not the gaps left while Python prepares the next launch
 PREQUEUE_CYCLES_PER_STEP = 200_000
 # batch chunks of the end-to-end (host buffers) measurement; each chunk's copies overlap the
-# other chunks' kernels
-E2E_CHUNKS = 2
+# other chunks' kernels (three: the library cuts 1 + 2 + 1 for c3, 4 + 8 + 4 for c5)
+E2E_CHUNKS = 3
 
 
 # ---------------------------------------------------------------------------- helpers

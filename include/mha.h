@@ -136,7 +136,10 @@ mha_status mha_set_workspace(mha_t handle, void* dev_ptr, size_t bytes);
  *          undefined, molayo1419.me pitfall 3)
  *   out    (B, T_q, D)
  * Needs a workspace of mha_workspace_size(B, T_q, T_kv) bytes.  Launches
- * three kernels (self) or four (cross) on `stream`.
+ * three kernels on `stream` (projection, attention, output projection; bf16 cross-
+ * attention with more than 128 query and 128 key rows projects both sides in one launch,
+ * see mha_linear_pair), four for other cross-attention, one more for the gate block of a
+ * gated cross-attention.
  * bf16 requires d_k == d_v in {64, 128} and D a multiple of 8 (else
  * MHA_ERR_UNSUPPORTED) and 16-byte aligned pointers (else MHA_ERR_INVALID_ARG);
  * fp32 accepts any shape with d_k, d_v <= 256.  B == 0 or T_q == 0 is a no-op;
@@ -180,7 +183,7 @@ mha_status mha_forward_ex(mha_t handle, const void* X_q, const void* X_kv, int B
 
 /*
  * mha_forward_host_workspace_size -- workspace bytes mha_forward_host needs: the forward's
- * scratch (mha_workspace_size) for one chunk of ceil(B / min(chunks, B)) batch elements,
+ * scratch (mha_workspace_size) for its largest chunk of batch elements (see mha_forward_host),
  * then device copies of X_q (B,T_q,D), X_kv (B,T_kv,D), the residual (B,T_q,D) and Y
  * (B,T_q,D), each 256-byte aligned.  0 for an invalid handle, a size <= 0 or chunks outside
  * [1, 16].
@@ -193,9 +196,11 @@ size_t mha_forward_host_workspace_size(mha_t handle, int B, int T_q, int T_kv, i
  * out are host pointers; W_qkv, b_qkv, W_o, b_o and kv_lengths stay device pointers
  * (resident weights).  Host buffers should be pinned (cudaHostAlloc/cudaHostRegister) for
  * the copies to run asynchronously.
- * The batch is cut into min(chunks, B) chunks of whole batch elements (every batch element
- * is an independent problem, so the result is the same as one mha_forward_ex over the
- * whole batch, bit for bit).  Chunk c's inputs go to the device on the handle's
+ * The batch is cut into at most min(chunks, B) chunks of whole batch elements (every batch
+ * element is an independent problem, so the result is the same as one mha_forward_ex over
+ * the whole batch, bit for bit): one or two chunks of ceil(B / n) elements; from three on,
+ * the first and last chunks half the size of the others (B = 4, chunks = 3: 1, 2, 1), so
+ * that the first copy-in and the last copy-out, which no kernel overlaps, are short.  Chunk c's inputs go to the device on the handle's
  * host-to-device stream, its forward runs on `stream` once they are in, and its output
  * goes back on the handle's device-to-host stream while chunk c+1 computes, so copies in
  * both directions overlap the kernels.  The copies start after the work already queued on
@@ -205,7 +210,7 @@ size_t mha_forward_host_workspace_size(mha_t handle, int B, int T_q, int T_kv, i
  * Needs a workspace of mha_forward_host_workspace_size(B, T_q, T_kv, chunks) bytes attached
  * on the current device (else MHA_ERR_WORKSPACE; another current device:
  * MHA_ERR_INVALID_ARG).  chunks outside [1, 16] is MHA_ERR_INVALID_ARG; other arguments as
- * for mha_forward_ex.  Launches 3 (self) or 4 (cross) kernels per chunk.
+ * for mha_forward_ex.  Launches the kernels of mha_forward_ex once per chunk.
  */
 mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int B, int T_q,
                             int T_kv, const void* W_qkv, const void* b_qkv, const void* W_o,

@@ -215,7 +215,8 @@ def test_forward_host_workspace_layout(lib):
     try:
         B, T, D = 4, 2048, 1024
         act = B * T * D * 2
-        # chunk scratch (for ceil(B / chunks) batch elements) + X_q, X_kv, residual, Y copies
+        # chunk scratch (for the largest chunk: 4; 2 + 2; 1 + 2 + 1; 1 each) + X_q, X_kv, residual,
+        # Y copies
         for chunks, Bc in ((1, 4), (2, 2), (3, 2), (4, 1), (16, 1)):
             assert L.mha_forward_host_workspace_size(hdl, B, T, T, chunks) == \
                 L.mha_workspace_size(hdl, Bc, T, T) + 4 * act

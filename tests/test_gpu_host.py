@@ -83,7 +83,7 @@ def _oracle(x, h, d, causal, residual):
 def test_host_forward_self_causal(dtype, d, chunks):
     h = 4
     D = h * d
-    B, T = 5, 200 if dtype == "bf16" else 40   # 5 batch elements: chunks of 3+2, 2+2+1, 1 each
+    B, T = 5, 200 if dtype == "bf16" else 40   # 5 batch elements: chunks of 3+2, 1+3+1, 1 each
     x = _case(90, dtype, B, T, D, h, d)
     got, dev = _run(x, dtype, D, h, d, True, None, chunks)
     assert torch.equal(got.view(torch.int16 if dtype == "bf16" else torch.int32),

@@ -256,11 +256,38 @@ struct HostLayout {
     size_t x_off, xkv_off, r_off, y_off, total;
 };
 
+// The batch cut of mha_forward_host: chunk c covers batch elements [bnd[c], bnd[c + 1]);
+// returns the number of chunks.  Up to two chunks are equal (ceil(B / n) elements); from three
+// on, the first and the last are half the size of the others, so that the copy-in before the
+// first kernel and the copy-out after the last one, which nothing overlaps, are short.
+int chunk_bounds(int B, int n, int* bnd) {
+    int k = 0;
+    bnd[0] = 0;
+    if (n <= 2) {
+        const int Bc = (B + n - 1) / n;
+        for (int b = Bc; b < B; b += Bc) bnd[++k] = b;
+        bnd[++k] = B;
+        return k;
+    }
+    double cum = 0.0;
+    for (int c = 0; c < n; ++c) {
+        cum += (c == 0 || c == n - 1) ? 0.5 : 1.0;
+        int e = (int)((double)B * cum / (n - 1) + 0.5);
+        if (e > B) e = B;
+        if (e > bnd[k]) bnd[++k] = e;
+    }
+    if (bnd[k] < B) bnd[++k] = B;
+    return k;
+}
+
 bool host_layout(const mha_s* m, int B, int T_q, int T_kv, int chunks, HostLayout* L) {
     if (B <= 0 || T_q <= 0 || T_kv <= 0 || chunks < 1 || chunks > kHostMaxChunks) return false;
     const int c = chunks < B ? chunks : B;
-    L->Bc = (B + c - 1) / c;
-    L->chunks = (B + L->Bc - 1) / L->Bc;
+    int bnd[kHostMaxChunks + 2];
+    L->chunks = chunk_bounds(B, c, bnd);
+    L->Bc = 0;  // the largest chunk
+    for (int i = 0; i < L->chunks; ++i)
+        if (bnd[i + 1] - bnd[i] > L->Bc) L->Bc = bnd[i + 1] - bnd[i];
     const size_t s = elem_bytes(m->dtype);
     const size_t xq = (size_t)B * T_q * (size_t)m->D * s, xkv = (size_t)B * T_kv * (size_t)m->D * s;
     L->x_off = align256(ws_layout(m, L->Bc, T_q, T_kv).total);
@@ -664,6 +691,8 @@ mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int
     if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
     if (dev != m->aux_dev) return MHA_ERR_INVALID_ARG;
 
+    int cb[kHostMaxChunks + 2];
+    chunk_bounds(B, chunks < B ? chunks : B, cb);
     uint8_t* ws = static_cast<uint8_t*>(m->ws);
     uint8_t* xd = ws + L.x_off;
     uint8_t* xkvd = ws + L.xkv_off;
@@ -677,7 +706,7 @@ mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int
         return MHA_ERR_CUDA;
     // inputs, chunk by chunk, on the host-to-device stream
     for (int c = 0; c < L.chunks; ++c) {
-        const int b0 = c * L.Bc, nb = (B - b0) < L.Bc ? (B - b0) : L.Bc;
+        const int b0 = cb[c], nb = cb[c + 1] - cb[c];
         const size_t oq = (size_t)b0 * T_q * row_q, nq = (size_t)nb * T_q * row_q;
         if (!cuda(cudaMemcpyAsync(xd + oq, static_cast<const uint8_t*>(X_q) + oq, nq, cudaMemcpyHostToDevice,
                                   m->aux_h2d)))
@@ -697,7 +726,7 @@ mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int
     // each chunk's forward on the caller's stream once its inputs are in; its output back on
     // the device-to-host stream while the next chunk computes
     for (int c = 0; c < L.chunks; ++c) {
-        const int b0 = c * L.Bc, nb = (B - b0) < L.Bc ? (B - b0) : L.Bc;
+        const int b0 = cb[c], nb = cb[c + 1] - cb[c];
         const size_t oq = (size_t)b0 * T_q * row_q, nq = (size_t)nb * T_q * row_q;
         if (!cuda(cudaStreamWaitEvent(cs, m->aux_in[c], 0))) return MHA_ERR_CUDA;
         st = mha_forward_ex(m, xd + oq, self ? nullptr : xkvd + (size_t)b0 * T_kv * row_q, nb, T_q, T_kv,

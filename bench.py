@@ -409,6 +409,12 @@ def measure_workload(w, K, warmup, torch, dev, world, flush, sampler=None):
                         "in chunks whose host-device copies overlap the kernels; weights resident"},
         "launches_per_step": launches_per_step(w), "wall": wall, "peak": pk["bf16_tflops"],
         "step_ms": step_stats(step_ms),
+        # the step's algorithmic HBM bytes (X in, Q/K/V and Ocat written and read back, Y out,
+        # the weights once; nominal key counts) over its time, against the measured copy rate
+        "hbm": {"algorithmic_bytes_per_step": wl.hbm_bytes(w),
+                "achieved_gbs": round(world * wl.hbm_bytes(w) / (ms_per_step / 1e3) / 1e9, 1),
+                "peak_gbs": pk["hbm_gbs"],
+                "frac": round(wl.hbm_bytes(w) / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
         "peak_source": pk_src,
     }
 
@@ -473,6 +479,7 @@ def run_ours(args):
         "e2e": r["e2e"],
         "gpu_launches": r["launches_per_step"] * K,
         "step_ms": r["step_ms"],
+        "hbm": r["hbm"],
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(r["wall"], 3),
     }
@@ -490,7 +497,7 @@ def run_ours(args):
                 "flops_counted": o["flops_counted"], "nominal_flops_per_step": o["nominal_flops"],
                 "config": {"B": ow.B, "T_q": ow.T_q, "T_kv": ow.T_kv, "D": ow.D, "h": ow.h,
                            "d_k": ow.d_k, "causal": ow.causal, "cross": ow.cross},
-                "roofline": o["roofline"], "e2e": o["e2e"], "step_ms": o["step_ms"],
+                "roofline": o["roofline"], "e2e": o["e2e"], "step_ms": o["step_ms"], "hbm": o["hbm"],
                 "clocks": s2.summary(), "steps": K, "warmup": args.warmup}
         line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

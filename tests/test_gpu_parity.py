@@ -76,6 +76,38 @@ def test_linear_step(dtype, M, K, N, bias):
     assert_close(to_host(C), oracle.linear(A, W, b), dtype, f"linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("M,K,N,residual", [
+    (32, 1024, 3072, False),    # a decode step's QKV projection: 12 tiles, clusters of 8
+    (100, 1032, 520, True),     # K tail inside a 64-wide block, N tail; 6 ranks of 3 K blocks
+    (128, 4096, 1024, True),    # 4 tiles, 8 ranks of 8 K blocks
+    (1, 2048, 12288, False),    # one row, 48 tiles, clusters of 2
+    (7, 136, 264, False),       # three K blocks over three ranks; N tail
+    (64, 512, 16384, True),     # 64 tiles, clusters of 2
+    (16, 512, 33024, False),    # 129 tiles: one CTA per tile
+])
+def test_linear_step_bf16_few_rows(M, K, N, residual):
+    """bf16 projections of at most 128 rows, where clusters of CTAs split K and add their
+    partial tiles through distributed shared memory: C = A W + bias (+ R) equals the oracle's
+    (the residual form adds R in the same epilogue), and a second call gives the same bits (the
+    partials are added in rank order)."""
+    A = wl.random_tensor((M, K), seed=41, dtype="bf16")
+    W = wl.random_tensor((K, N), seed=42, dtype="bf16", scale=0.5 / np.sqrt(K))
+    b = wl.random_tensor((N,), seed=43, dtype="bf16", scale=0.1)
+    R = wl.random_tensor((M, N), seed=44, dtype="bf16") if residual else None
+    layer = Mha(64, 1, 64, dtype=torch.bfloat16)
+    layer.ensure_workspace(1, 1, 1)
+    Ad, Wd, bd, Rd = (to_device(t, "bf16") for t in (A, W, b, R))
+    C1 = layer.linear(Ad, Wd, bd, residual=Rd)
+    C2 = layer.linear(Ad, Wd, bd, residual=Rd)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    ref = oracle.linear(A, W, b)
+    if residual:
+        ref = ref + R.astype(np.float64)  # already bf16 values
+    assert_close(to_host(C1), ref, "bf16", f"few-row linear {M}x{K}x{N}")
+    assert torch.equal(C1, C2), "a second call gave a different result"
+
+
 @pytest.mark.parametrize("M,K,N", [(70, 37, 45), (129, 130, 67), (64, 33, 64)])
 def test_linear_step_f32_unaligned(M, K, N):
     """fp32 projections whose row strides are not a multiple of four floats take the scalar

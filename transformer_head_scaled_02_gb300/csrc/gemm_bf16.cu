@@ -45,6 +45,7 @@ constexpr int G_THREADS = 192;
 constexpr uint32_t G_TMEM_COLS = 512;
 
 static_assert(G_SMEM <= 232448, "shared memory budget");
+constexpr int SK_SMEM = G_STAGES * (G_A_BYTES + G_B_BYTES) + G_BAR_BYTES + 1024;
 
 // Bounded wait that ignores the abort flag: used only to drain copies / MMAs still in
 // flight before the CTA exits.
@@ -355,6 +356,210 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// At most 128 rows (the new tokens of a decode step) over few column tiles: the one-CTA kernel
+// above reads all of W through a handful of SMs.  Here a cluster of S CTAs shares one 128 x 256
+// tile: CTA r (its rank) runs the K blocks [r * kb_per, (r + 1) * kb_per), puts its fp32 partial
+// tile into its own (by then idle) stage buffers, and after a cluster barrier reduces columns
+// [r * 256 / S, (r + 1) * 256 / S) of the tile over all S partials, read in rank order through
+// distributed shared memory (so the sum does not depend on timing), adds bias and residual and
+// writes C.  A second cluster barrier keeps every partial alive until its readers are done.
+// Roles as above (warp 0 TMA, warp 1 MMA, warps 2..5 epilogue); all six warps reduce.
+// Partial layout: row r at r * 1 KB, its 64 groups of four columns as float4s, the low three bits
+// of the group index XORed with r & 7 so that the eight rows a quarter-warp writes hit
+// different banks.
+__global__ void __launch_bounds__(G_THREADS, 1)
+    gemm_bf16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmW,
+                            const __nv_bfloat16* __restrict__ bias,
+                            const __nv_bfloat16* __restrict__ R, int64_t ldr,
+                            __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K,
+                            int kb_per, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + G_STAGES * G_A_BYTES;
+    const uint32_t sBar = sB + G_STAGES * G_B_BYTES;
+    const uint32_t sPart = base;  // the partial tile reuses the stage buffers (<= 128 KB)
+    // barriers: full[S], empty[S], tfull, drain
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8u * G_STAGES;
+    const uint32_t bar_tfull = sBar + 16u * G_STAGES;
+    const uint32_t bar_drain = bar_tfull + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n0 = (int)blockIdx.x * G_BN;
+    const int S = (int)gridDim.y;  // the cluster spans the whole y extent
+    const int rank = (int)cluster_ctarank();
+    const int num_k = (K + G_BK - 1) / G_BK;
+    const int kb0 = rank * kb_per;
+    const int kb1 = min(num_k, kb0 + kb_per);  // the host makes every range non-empty
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < G_STAGES; ++st) {
+            mbar_init(bar_full + 8u * st, 1);
+            mbar_init(bar_empty + 8u * st, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (rows past M arrive as zeros)
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) break;
+                const uint32_t fb = bar_full + 8u * stage;
+                mbar_arrive_expect_tx(fb, G_A_BYTES + G_B_BYTES);
+                tma_load_2d(sA + stage * G_A_BYTES, &tmA, kb * G_BK, 0, fb);
+#pragma unroll
+                for (int c = 0; c < G_BN / 64; ++c)
+                    tma_load_2d(sB + stage * G_B_BYTES + c * G_B_CHUNK, &tmW, n0 + c * 64, kb * G_BK, fb);
+                ++issued;
+                if (++stage == G_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            for (int back = 0; back < G_STAGES && back < issued; ++back) {
+                stage = stage == 0 ? G_STAGES - 1 : stage - 1;
+                if (stage == G_STAGES - 1) phase ^= 1u;
+                drain_wait(bar_full + 8u * stage, phase);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(G_BM, G_BN, false, true);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(bar_full + 8u * stage, phase, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sA + stage * G_A_BYTES;
+                const uint32_t b0 = sB + stage * G_B_BYTES;
+#pragma unroll
+                for (int k = 0; k < G_BK / 16; ++k) {
+                    const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(b0 + k * 2048, G_B_CHUNK, 1024);
+                    mma_bf16_ss(tmem_base, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                }
+                tc_commit(bar_empty + 8u * stage);
+                if (++stage == G_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) tc_commit(bar_tfull);
+            tc_commit(bar_drain);
+            drain_wait(bar_drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, thread = row q * 32 + lane of the tile.  Once
+        // the accumulator is complete every MMA has read its operands and every load has
+        // landed, so the stage buffers are free for the partial.
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16);
+        if (__all_sync(0xffffffffu, mbar_wait(bar_tfull, 0, abort_flag, status))) {
+            tc_fence_after();
+            const uint32_t prow = sPart + (uint32_t)row * 1024u;
+            const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll 1
+            for (int c = 0; c < G_BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t0 + c * 32, v);
+                tmem_wait_ld();
+                if (row < M)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(prow + (((uint32_t)(c * 8) + ((uint32_t)u ^ sw)) << 4), v[4 * u],
+                                     v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+        }
+    }
+
+    // every thread of every CTA of the cluster passes both barriers, whatever its role did
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    {
+        // ---------------- reduction of this rank's column groups [g0, g1) over the S partials
+        const int gs = (64 + S - 1) / S;
+        const int g0 = rank * gs;
+        const int w = min(64, g0 + gs) - g0;
+        const int count = w > 0 ? M * w : 0;
+#pragma unroll 1
+        for (int e = threadIdx.x; e < count; e += G_THREADS) {
+            const int row = e / w;
+            const int g = g0 + e % w;
+            const int n = n0 + g * 4;
+            if (n >= N) continue;  // N is a multiple of 8: a group of four is all in or out
+            const uint32_t off = (uint32_t)row * 1024u + ((uint32_t)((g & ~7) | ((g ^ row) & 7)) << 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (r < S) {
+                    const float4 p = ld_shared_cluster_v4(mapa_shared(sPart + off, (uint32_t)r));
+                    acc.x += p.x;
+                    acc.y += p.y;
+                    acc.z += p.z;
+                    acc.w += p.w;
+                }
+            }
+            if (bias != nullptr) {
+                const uint2 bb = *reinterpret_cast<const uint2*>(bias + n);
+                acc.x += __uint_as_float(bb.x << 16);
+                acc.y += __uint_as_float(bb.x & 0xffff0000u);
+                acc.z += __uint_as_float(bb.y << 16);
+                acc.w += __uint_as_float(bb.y & 0xffff0000u);
+            }
+            if (R != nullptr) {
+                const uint2 rr = *reinterpret_cast<const uint2*>(R + (int64_t)row * ldr + n);
+                acc.x += __uint_as_float(rr.x << 16);
+                acc.y += __uint_as_float(rr.x & 0xffff0000u);
+                acc.z += __uint_as_float(rr.y << 16);
+                acc.w += __uint_as_float(rr.y & 0xffff0000u);
+            }
+            *reinterpret_cast<uint2*>(C + (int64_t)row * ldc + n) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
+    }
+    __syncwarp();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 256);
+    }
+}
 
 // ---------------------------------------------------------------------------------------
 // CTA-pair version (cta_group::2): a cluster of two CTAs on two SMs computes a 256x256
@@ -956,6 +1161,64 @@ bool encode_pair_maps(const void* A, int64_t lda, const void* W, int64_t ldw, vo
            encode_tmap_bf16(tC, C, 2, dc, sc, bc);
 }
 
+// Clusters of S CTAs share each tile of a projection of at most 128 rows: returns S (0: one
+// CTA per tile instead) and the K blocks of each rank.  About 128 CTAs in all, at most 8 to a
+// cluster (the portable limit), every rank at least one K block.
+int splitk_plan(int M, int N, int K, int* kb_per) {
+    if (M <= 0 || M > G_BM || N <= 0 || K <= 0) return 0;
+    const int tiles = (N + G_BN - 1) / G_BN, num_k = (K + G_BK - 1) / G_BK;
+    int S = 128 / tiles;
+    if (S > 8) S = 8;
+    if (S > num_k) S = num_k;
+    if (S < 2) return 0;
+    const int per = (num_k + S - 1) / S;
+    S = (num_k + per - 1) / per;
+    if (S < 2) return 0;
+    *kb_per = per;
+    return S;
+}
+
+cudaError_t launch_splitk(const CUtensorMap& tA, const CUtensorMap& tW, const void* bias,
+                          const void* R, int64_t ldr, void* C, int64_t ldc, int M, int N, int K,
+                          int S, int kb_per, int* status, cudaStream_t stream, bool* launched) {
+    *launched = false;
+    cudaError_t err = cudaFuncSetAttribute(gemm_bf16_splitk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + G_BN - 1) / G_BN, S);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = SK_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a cluster of S CTAs of this size must fit on the device at all (cached per device and S)
+    static int fits[64][9];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+    int& f = fits[dev >= 0 && dev < 64 ? dev : 0][S];
+    if (f == 0) {
+        int n = 0;
+        f = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_splitk_kernel, &cfg) == cudaSuccess && n > 0 ? 1 : -1;
+        cudaGetLastError();
+    }
+    if (f < 0) return cudaSuccess;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, gemm_bf16_splitk_kernel, tA, tW,
+                             reinterpret_cast<const __nv_bfloat16*>(bias),
+                             reinterpret_cast<const __nv_bfloat16*>(R), ldr,
+                             static_cast<__nv_bfloat16*>(C), ldc, M, N, K, kb_per, status);
+    *launched = err == cudaSuccess;
+    return err;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_bf16_two(const void* A, int64_t lda, const void* W, int64_t ldw,
@@ -1066,6 +1329,15 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
                           reinterpret_cast<const __nv_bfloat16*>(R), ldr, M, N, K, status,
                           listed ? seg_len : nullptr, listed ? seg_rows : 0, tA, tW, tC,
                           static_cast<const __nv_bfloat16*>(nullptr), 0, 0);
+    }
+    int kb_per = 0;
+    const int S = splitk_plan(M, N, K, &kb_per);
+    if (S > 0) {
+        // few rows: clusters of S CTAs split K (every row is written, seg_len or not)
+        bool launched = false;
+        const cudaError_t err = launch_splitk(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status,
+                                              stream, &launched);
+        if (err != cudaSuccess || launched) return err;
     }
     cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);

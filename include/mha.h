@@ -223,7 +223,9 @@ mha_status mha_forward_host(mha_t handle, const void* X_q, const void* X_kv, int
  *   A (M, K) row stride lda;  W (K, N) row stride ldw;  bias (N) or NULL;
  *   C (M, N) row stride ldc.   fp32 accumulate in both dtypes.
  * bf16 requires K, N, lda, ldw, ldc multiples of 8 and 16-byte aligned
- * pointers.  M, N, K >= 1.
+ * pointers.  M, N, K >= 1.  bf16 with M <= 128 (a decode step's new tokens) splits K over a
+ * cluster of CTAs per output tile and adds their fp32 partials in a fixed order: the result is
+ * the same on every call, and differs from the unsplit sum only by fp32 rounding.
  */
 mha_status mha_linear(mha_t handle, const void* A, int64_t lda, int M, int K,
                       const void* W, int64_t ldw, int N, const void* bias,

@@ -77,13 +77,13 @@ def test_linear_step(dtype, M, K, N, bias):
 
 
 @pytest.mark.parametrize("M,K,N,residual", [
-    (32, 1024, 3072, False),    # a decode step's QKV projection: 12 tiles, clusters of 8
+    (32, 1024, 3072, False),    # a decode step's QKV projection: 24 tiles, clusters of 4
     (100, 1032, 520, True),     # K tail inside a 64-wide block, N tail; 6 ranks of 3 K blocks
-    (128, 4096, 1024, True),    # 4 tiles, 8 ranks of 8 K blocks
-    (1, 2048, 12288, False),    # one row, 48 tiles, clusters of 2
+    (128, 4096, 1024, True),    # 8 tiles, 8 ranks of 8 K blocks
+    (1, 2048, 12288, False),    # one row; 96 tiles of 128 columns: 48 of 256 in clusters of 2
     (7, 136, 264, False),       # three K blocks over three ranks; N tail
-    (64, 512, 16384, True),     # 64 tiles, clusters of 2
-    (16, 512, 33024, False),    # 129 tiles: one CTA per tile
+    (64, 512, 16384, True),     # 64 tiles of 256 columns in clusters of 2
+    (16, 512, 33024, False),    # 129 tiles of 256 columns: one CTA per tile
 ])
 def test_linear_step_bf16_few_rows(M, K, N, residual):
     """bf16 projections of at most 128 rows, where clusters of CTAs split K and add their

@@ -45,7 +45,8 @@ constexpr int G_THREADS = 192;
 constexpr uint32_t G_TMEM_COLS = 512;
 
 static_assert(G_SMEM <= 232448, "shared memory budget");
-constexpr int SK_SMEM = G_STAGES * (G_A_BYTES + G_B_BYTES) + G_BAR_BYTES + 1024;
+template <int BN>
+constexpr int sk_smem() { return G_STAGES * (G_A_BYTES + G_BK * BN * 2) + G_BAR_BYTES + 1024; }
 
 // Bounded wait that ignores the abort flag: used only to drain copies / MMAs still in
 // flight before the CTA exits.
@@ -359,16 +360,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
 // ---------------------------------------------------------------------------------------
 // At most 128 rows (the new tokens of a decode step) over few column tiles: the one-CTA kernel
-// above reads all of W through a handful of SMs.  Here a cluster of S CTAs shares one 128 x 256
-// tile: CTA r (its rank) runs the K blocks [r * kb_per, (r + 1) * kb_per), puts its fp32 partial
-// tile into its own (by then idle) stage buffers, and after a cluster barrier reduces columns
-// [r * 256 / S, (r + 1) * 256 / S) of the tile over all S partials, read in rank order through
-// distributed shared memory (so the sum does not depend on timing), adds bias and residual and
-// writes C.  A second cluster barrier keeps every partial alive until its readers are done.
-// Roles as above (warp 0 TMA, warp 1 MMA, warps 2..5 epilogue); all six warps reduce.
-// Partial layout: row r at r * 1 KB, its 64 groups of four columns as float4s, the low three bits
-// of the group index XORed with r & 7 so that the eight rows a quarter-warp writes hit
-// different banks.
+// above reads all of W through a handful of SMs.  Here a cluster of S CTAs shares one 128 x BN
+// tile (BN a multiple of 64; launched with 128): CTA r (its rank) runs the K blocks
+// [r * kb_per, (r + 1) * kb_per), puts its fp32 partial tile into its own (by then idle) stage
+// buffers, and after a cluster barrier reduces columns [r * BN / S, (r + 1) * BN / S) of the
+// tile over all S partials, read in rank order through distributed shared memory (so the sum
+// does not depend on timing), adds bias and residual and writes C.  A second cluster barrier
+// keeps every partial alive until its readers are done.  Roles as above (warp 0 TMA, warp 1
+// MMA, warps 2..5 epilogue); all six warps reduce.  Distributed shared memory moves only
+// ~20-30 GB/s into each SM (measured, by loads, stores or bulk copies alike), so the exchange,
+// M x BN x 4 x (S - 1) / S bytes per rank, is what bounds this kernel from a few dozen rows up.
+// Partial layout: row r at r * BN * 4 bytes, its BN / 4 groups of four columns as float4s,
+// the low three bits of the group index XORed with r & 7 so that the eight rows a
+// quarter-warp writes hit different banks.
+template <int BN>
 __global__ void __launch_bounds__(G_THREADS, 1)
     gemm_bf16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmW,
@@ -376,6 +381,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                             const __nv_bfloat16* __restrict__ R, int64_t ldr,
                             __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K,
                             int kb_per, int* status) {
+    constexpr int B_BYTES = G_BK * BN * 2;  // W stage: BN / 64 chunks of 64 columns
+    constexpr int GROUPS = BN / 4;          // float4 column groups of a partial row
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
     const uint32_t sA = base;
     const uint32_t sB = sA + G_STAGES * G_A_BYTES;
-    const uint32_t sBar = sB + G_STAGES * G_B_BYTES;
+    const uint32_t sBar = sB + G_STAGES * B_BYTES;
     const uint32_t sPart = base;  // the partial tile reuses the stage buffers (<= 128 KB)
     // barriers: full[S], empty[S], tfull, drain
     const uint32_t bar_full = sBar;
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = (int)blockIdx.x * G_BN;
+    const int n0 = (int)blockIdx.x * BN;
     const int S = (int)gridDim.y;  // the cluster spans the whole y extent
     const int rank = (int)cluster_ctarank();
     const int num_k = (K + G_BK - 1) / G_BK;
@@ -415,7 +422,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), BN);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -434,11 +441,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) break;
                 const uint32_t fb = bar_full + 8u * stage;
-                mbar_arrive_expect_tx(fb, G_A_BYTES + G_B_BYTES);
+                mbar_arrive_expect_tx(fb, G_A_BYTES + B_BYTES);
                 tma_load_2d(sA + stage * G_A_BYTES, &tmA, kb * G_BK, 0, fb);
 #pragma unroll
-                for (int c = 0; c < G_BN / 64; ++c)
-                    tma_load_2d(sB + stage * G_B_BYTES + c * G_B_CHUNK, &tmW, n0 + c * 64, kb * G_BK, fb);
+                for (int c = 0; c < BN / 64; ++c)
+                    tma_load_2d(sB + stage * B_BYTES + c * G_B_CHUNK, &tmW, n0 + c * 64, kb * G_BK, fb);
                 ++issued;
                 if (++stage == G_STAGES) {
                     stage = 0;
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            const uint32_t idesc = idesc_bf16_f32(G_BM, G_BN, false, true);
+            const uint32_t idesc = idesc_bf16_f32(G_BM, BN, false, true);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t a0 = sA + stage * G_A_BYTES;
-                const uint32_t b0 = sB + stage * G_B_BYTES;
+                const uint32_t b0 = sB + stage * B_BYTES;
 #pragma unroll
                 for (int k = 0; k < G_BK / 16; ++k) {
                     const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
@@ -491,10 +498,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16);
         if (__all_sync(0xffffffffu, mbar_wait(bar_tfull, 0, abort_flag, status))) {
             tc_fence_after();
-            const uint32_t prow = sPart + (uint32_t)row * 1024u;
+            const uint32_t prow = sPart + (uint32_t)(row * BN * 4);
             const uint32_t sw = (uint32_t)(row & 7);
 #pragma unroll 1
-            for (int c = 0; c < G_BN / 32; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t0 + c * 32, v);
                 tmem_wait_ld();
@@ -513,9 +520,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     cluster_sync_all();
     {
         // ---------------- reduction of this rank's column groups [g0, g1) over the S partials
-        const int gs = (64 + S - 1) / S;
+        const int gs = (GROUPS + S - 1) / S;
         const int g0 = rank * gs;
-        const int w = min(64, g0 + gs) - g0;
+        const int w = min(GROUPS, g0 + gs) - g0;
         const int count = w > 0 ? M * w : 0;
 #pragma unroll 1
         for (int e = threadIdx.x; e < count; e += G_THREADS) {
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const int g = g0 + e % w;
             const int n = n0 + g * 4;
             if (n >= N) continue;  // N is a multiple of 8: a group of four is all in or out
-            const uint32_t off = (uint32_t)row * 1024u + ((uint32_t)((g & ~7) | ((g ^ row) & 7)) << 4);
+            const uint32_t off = (uint32_t)(row * BN * 4) + ((uint32_t)((g & ~7) | ((g ^ row) & 7)) << 4);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 256);
+        tmem_dealloc(tmem_base, BN);
     }
 }
 
@@ -1161,15 +1168,49 @@ bool encode_pair_maps(const void* A, int64_t lda, const void* W, int64_t ldw, vo
            encode_tmap_bf16(tC, C, 2, dc, sc, bc);
 }
 
-// Clusters of S CTAs share each tile of a projection of at most 128 rows: returns S (0: one
-// CTA per tile instead) and the K blocks of each rank.  About 128 CTAs in all, at most 8 to a
-// cluster (the portable limit), every rank at least one K block.
+// Clusters of S CTAs of the split kernel that the device runs at once (0: none), per device,
+// tile width and S.
+template <int BN>
+int splitk_max_clusters(int S) {
+    static int cache[64][9];  // count + 1; 0 = not asked yet
+    int dev = -1;
+    if (S < 1 || S > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int& c = cache[dev][S];
+    if (c == 0) {
+        int n = 0;
+        if (cudaFuncSetAttribute(gemm_bf16_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 sk_smem<BN>()) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, S);
+            cfg.blockDim = dim3(G_THREADS);
+            cfg.dynamicSmemBytes = sk_smem<BN>();
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = (unsigned)S;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_splitk_kernel<BN>, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        c = n + 1;
+    }
+    return c - 1;
+}
+
+// Clusters of S CTAs share each 128 x BN tile of a projection of at most 128 rows: returns S
+// (0: one CTA per 256-column tile of the kernel above instead) and the K blocks of each rank.  About 128 CTAs in
+// all, at most 8 to a cluster (the portable limit), no more clusters than the device runs at
+// once (a second wave of clusters would double the time), every rank at least one K block.
+template <int BN>
 int splitk_plan(int M, int N, int K, int* kb_per) {
     if (M <= 0 || M > G_BM || N <= 0 || K <= 0) return 0;
-    const int tiles = (N + G_BN - 1) / G_BN, num_k = (K + G_BK - 1) / G_BK;
+    const int tiles = (N + BN - 1) / BN, num_k = (K + G_BK - 1) / G_BK;
     int S = 128 / tiles;
     if (S > 8) S = 8;
     if (S > num_k) S = num_k;
+    while (S >= 2 && tiles > splitk_max_clusters<BN>(S)) --S;
     if (S < 2) return 0;
     const int per = (num_k + S - 1) / S;
     S = (num_k + per - 1) / per;
@@ -1178,17 +1219,17 @@ int splitk_plan(int M, int N, int K, int* kb_per) {
     return S;
 }
 
+template <int BN>
 cudaError_t launch_splitk(const CUtensorMap& tA, const CUtensorMap& tW, const void* bias,
                           const void* R, int64_t ldr, void* C, int64_t ldc, int M, int N, int K,
-                          int S, int kb_per, int* status, cudaStream_t stream, bool* launched) {
-    *launched = false;
-    cudaError_t err = cudaFuncSetAttribute(gemm_bf16_splitk_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM);
+                          int S, int kb_per, int* status, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(gemm_bf16_splitk_kernel<BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, sk_smem<BN>());
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + G_BN - 1) / G_BN, S);
+    cfg.gridDim = dim3((N + BN - 1) / BN, S);
     cfg.blockDim = dim3(G_THREADS);
-    cfg.dynamicSmemBytes = SK_SMEM;
+    cfg.dynamicSmemBytes = sk_smem<BN>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1198,25 +1239,11 @@ cudaError_t launch_splitk(const CUtensorMap& tA, const CUtensorMap& tW, const vo
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // a cluster of S CTAs of this size must fit on the device at all (cached per device and S)
-    static int fits[64][9];
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
-    int& f = fits[dev >= 0 && dev < 64 ? dev : 0][S];
-    if (f == 0) {
-        int n = 0;
-        f = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_splitk_kernel, &cfg) == cudaSuccess && n > 0 ? 1 : -1;
-        cudaGetLastError();
-    }
-    if (f < 0) return cudaSuccess;
     cfg.numAttrs = 2;
-    err = cudaLaunchKernelEx(&cfg, gemm_bf16_splitk_kernel, tA, tW,
-                             reinterpret_cast<const __nv_bfloat16*>(bias),
-                             reinterpret_cast<const __nv_bfloat16*>(R), ldr,
-                             static_cast<__nv_bfloat16*>(C), ldc, M, N, K, kb_per, status);
-    *launched = err == cudaSuccess;
-    return err;
+    return cudaLaunchKernelEx(&cfg, gemm_bf16_splitk_kernel<BN>, tA, tW,
+                              reinterpret_cast<const __nv_bfloat16*>(bias),
+                              reinterpret_cast<const __nv_bfloat16*>(R), ldr,
+                              static_cast<__nv_bfloat16*>(C), ldc, M, N, K, kb_per, status);
 }
 
 }  // namespace
@@ -1330,15 +1357,15 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
                           listed ? seg_len : nullptr, listed ? seg_rows : 0, tA, tW, tC,
                           static_cast<const __nv_bfloat16*>(nullptr), 0, 0);
     }
+    // few rows: clusters of S CTAs split K over 128-column tiles (every row is written, seg_len
+    // or not).  128 columns rather than 256: each rank exchanges half the partial bytes, and
+    // measured 1-20% faster from 32 rows up, the same at one row.  Past 64 such tiles (N >
+    // 8192) 256-column tiles still leave room for clusters of two.
     int kb_per = 0;
-    const int S = splitk_plan(M, N, K, &kb_per);
-    if (S > 0) {
-        // few rows: clusters of S CTAs split K (every row is written, seg_len or not)
-        bool launched = false;
-        const cudaError_t err = launch_splitk(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status,
-                                              stream, &launched);
-        if (err != cudaSuccess || launched) return err;
-    }
+    int S = splitk_plan<128>(M, N, K, &kb_per);
+    if (S > 0) return launch_splitk<128>(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
+    S = splitk_plan<256>(M, N, K, &kb_per);
+    if (S > 0) return launch_splitk<256>(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
     cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (err != cudaSuccess) return err;

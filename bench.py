@@ -523,6 +523,7 @@ VARIANTS = {
     "decode-mha": dict(decode=True, h_kv=16),
     "decode-gqa4": dict(decode=True, h_kv=4),
     "decode-mqa": dict(decode=True, h_kv=1),
+    "decode-proj": dict(decode_proj=True),
 }
 DECODE_SHAPE = dict(B=32, T_q=1, T_max=8192, h=16, d=128)
 
@@ -556,6 +557,45 @@ def run_variant(args):
 
     def bf(shape, seed, scale=1.0):
         return to_device(wl.random_tensor(shape, seed, "bf16", scale), "bf16", torch)
+
+    if v.get("decode_proj"):
+        # the projections of the same decode step: B new tokens (one per sequence) through
+        # W_qkv and, with the residual, through W_O; weights read once per step
+        c = DECODE_SHAPE
+        M, D = c["B"] * c["T_q"], c["h"] * c["d"]
+        layer = Mha(D, c["h"], c["d"], c["d"], dtype=torch.bfloat16)
+        layer.ensure_workspace(1, 1, 1)
+        X = bf((M, D), 1)
+        Wqkv, bqkv = bf((D, 3 * D), 2, 0.02), bf((3 * D,), 3, 0.02)
+        Oc = bf((M, D), 4)
+        Wo, bo = bf((D, D), 5, 0.02), bf((D,), 6, 0.02)
+        qkv = torch.empty((M, 3 * D), dtype=torch.bfloat16, device=dev)
+        Y = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            layer.linear(X, Wqkv, bqkv, out=qkv)
+            layer.linear(Oc, Wo, bo, out=Y, residual=X)
+        sampler.start()
+        ms = _timed_steps(torch, fn, flush, args.steps, args.warmup)
+        sampler.stop()
+        if layer.status() != 0:
+            raise RuntimeError("device status reports an error")
+        weights = 2.0 * (D * 3 * D + D * D)
+        small = 2.0 * (3 * D + D + M * D * 3 + M * 3 * D + M * D)   # biases, X twice, Ocat, outputs
+        gbs = (weights + small) / (ms / 1e3) / 1e9
+        line = {"metric": "MHA decode step projections: weight read bandwidth", "value": round(gbs, 1),
+                "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) activations, N(0, 0.02^2) weights)",
+                "config": {"variant": args.variant, "rows": M, "D": D, "qkv": [M, D, 3 * D],
+                           "out_with_residual": [M, D, D], "weight_bytes": weights,
+                           "l2": "flushed before every timed step"},
+                "roofline": {"kernel": "gemm_bf16_splitk_kernel x 2", "bound": "hbm", "achieved": round(gbs, 1),
+                             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                             "peak_source": f"{pk_src} HBM copy"},
+                "gpu_launches": 2 * args.steps, "clocks": sampler.summary()}
+        print(json.dumps(line), flush=True)
+        return
 
     if v.get("decode"):
         c = DECODE_SHAPE

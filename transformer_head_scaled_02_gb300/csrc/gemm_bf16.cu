@@ -45,8 +45,6 @@ constexpr int G_THREADS = 192;
 constexpr uint32_t G_TMEM_COLS = 512;
 
 static_assert(G_SMEM <= 232448, "shared memory budget");
-template <int BN>
-constexpr int sk_smem() { return G_STAGES * (G_A_BYTES + G_BK * BN * 2) + G_BAR_BYTES + 1024; }
 
 // Bounded wait that ignores the abort flag: used only to drain copies / MMAs still in
 // flight before the CTA exits.
@@ -380,7 +378,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                             const __nv_bfloat16* __restrict__ bias,
                             const __nv_bfloat16* __restrict__ R, int64_t ldr,
                             __nv_bfloat16* __restrict__ C, int64_t ldc, int M, int N, int K,
-                            int kb_per, int* status) {
+                            int kb_per, int a_rows, int nst, int* status) {
     constexpr int B_BYTES = G_BK * BN * 2;  // W stage: BN / 64 chunks of 64 columns
     constexpr int GROUPS = BN / 4;          // float4 column groups of a partial row
     extern __shared__ uint8_t smem_raw[];
@@ -388,14 +386,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
 
-    const uint32_t sA = base;
-    const uint32_t sB = sA + G_STAGES * G_A_BYTES;
-    const uint32_t sBar = sB + G_STAGES * B_BYTES;
-    const uint32_t sPart = base;  // the partial tile reuses the stage buffers (<= 128 KB)
-    // barriers: full[S], empty[S], tfull, drain
+    // nst stages of [A: a_rows x 64 K][W: 64 K x BN].  The MMA reads 128 rows of A; those past
+    // a_rows (which hold no row below M) come from the stage's own W bytes, so they are
+    // complete when the stage is, and only fill accumulator rows that are never stored.
+    const uint32_t a_bytes = (uint32_t)a_rows * 128u;
+    const uint32_t stage_bytes = a_bytes + (uint32_t)B_BYTES;
+    const uint32_t sBar = base + (uint32_t)nst * stage_bytes;
+    const uint32_t sPart = base;  // the partial tile reuses the stage buffers (<= 64 KB)
+    // barriers: full[nst], empty[nst], tfull, drain
     const uint32_t bar_full = sBar;
-    const uint32_t bar_empty = sBar + 8u * G_STAGES;
-    const uint32_t bar_tfull = sBar + 16u * G_STAGES;
+    const uint32_t bar_empty = sBar + 8u * (uint32_t)nst;
+    const uint32_t bar_tfull = sBar + 16u * (uint32_t)nst;
     const uint32_t bar_drain = bar_tfull + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar_drain + 8u - base));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int kb1 = min(num_k, kb0 + kb_per);  // the host makes every range non-empty
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < G_STAGES; ++st) {
+        for (int st = 0; st < nst; ++st) {
             mbar_init(bar_full + 8u * st, 1);
             mbar_init(bar_empty + 8u * st, 1);
         }
@@ -441,20 +442,21 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u, abort_flag, status)) break;
                 const uint32_t fb = bar_full + 8u * stage;
-                mbar_arrive_expect_tx(fb, G_A_BYTES + B_BYTES);
-                tma_load_2d(sA + stage * G_A_BYTES, &tmA, kb * G_BK, 0, fb);
+                const uint32_t st0 = base + (uint32_t)stage * stage_bytes;
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                tma_load_2d(st0, &tmA, kb * G_BK, 0, fb);
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c)
-                    tma_load_2d(sB + stage * B_BYTES + c * G_B_CHUNK, &tmW, n0 + c * 64, kb * G_BK, fb);
+                    tma_load_2d(st0 + a_bytes + c * G_B_CHUNK, &tmW, n0 + c * 64, kb * G_BK, fb);
                 ++issued;
-                if (++stage == G_STAGES) {
+                if (++stage == nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
-            for (int back = 0; back < G_STAGES && back < issued; ++back) {
-                stage = stage == 0 ? G_STAGES - 1 : stage - 1;
-                if (stage == G_STAGES - 1) phase ^= 1u;
+            for (int back = 0; back < nst && back < issued; ++back) {
+                stage = stage == 0 ? nst - 1 : stage - 1;
+                if (stage == nst - 1) phase ^= 1u;
                 drain_wait(bar_full + 8u * stage, phase);
             }
         }
@@ -471,8 +473,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sA + stage * G_A_BYTES;
-                const uint32_t b0 = sB + stage * B_BYTES;
+                const uint32_t a0 = base + (uint32_t)stage * stage_bytes;
+                const uint32_t b0 = a0 + a_bytes;
 #pragma unroll
                 for (int k = 0; k < G_BK / 16; ++k) {
                     const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     mma_bf16_ss(tmem_base, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
                 }
                 tc_commit(bar_empty + 8u * stage);
-                if (++stage == G_STAGES) {
+                if (++stage == nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -1168,6 +1170,18 @@ bool encode_pair_maps(const void* A, int64_t lda, const void* W, int64_t ldw, vo
            encode_tmap_bf16(tC, C, 2, dc, sc, bc);
 }
 
+// Shared memory of the split kernel: up to 8 stages of (A rows rounded up to 8) x 64 K plus
+// 64 K x BN of W, within the per-CTA limit.  Every launch takes more than half an SM's shared
+// memory (at least 8 x 17 KB), so one CTA runs per SM whatever the row count.
+constexpr int SK_SMEM_MAX = 232448;
+constexpr int SK_SMEM_EXTRA = G_BAR_BYTES + 1024;
+template <int BN>
+int splitk_stages(int a_rows) {
+    const int stage = a_rows * 128 + G_BK * BN * 2;
+    const int n = (SK_SMEM_MAX - SK_SMEM_EXTRA) / stage;
+    return n < 8 ? n : 8;
+}
+
 // Clusters of S CTAs of the split kernel that the device runs at once (0: none), per device,
 // tile width and S.
 template <int BN>
@@ -1179,11 +1193,11 @@ int splitk_max_clusters(int S) {
     if (c == 0) {
         int n = 0;
         if (cudaFuncSetAttribute(gemm_bf16_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 sk_smem<BN>()) == cudaSuccess) {
+                                 SK_SMEM_MAX) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(1, S);
             cfg.blockDim = dim3(G_THREADS);
-            cfg.dynamicSmemBytes = sk_smem<BN>();
+            cfg.dynamicSmemBytes = SK_SMEM_MAX;  // one CTA per SM, as every launch
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = 1;
@@ -1200,14 +1214,15 @@ int splitk_max_clusters(int S) {
 }
 
 // Clusters of S CTAs share each 128 x BN tile of a projection of at most 128 rows: returns S
-// (0: one CTA per 256-column tile of the kernel above instead) and the K blocks of each rank.  About 128 CTAs in
-// all, at most 8 to a cluster (the portable limit), no more clusters than the device runs at
-// once (a second wave of clusters would double the time), every rank at least one K block.
+// (0: one CTA per 256-column tile of the kernel above instead) and the K blocks of each rank.
+// About one CTA per SM in all, at most 8 to a cluster (the portable limit), no more clusters
+// than the device runs at once (a second wave of clusters would double the time), every rank
+// at least one K block.
 template <int BN>
-int splitk_plan(int M, int N, int K, int* kb_per) {
+int splitk_plan(int M, int N, int K, int num_sms, int* kb_per) {
     if (M <= 0 || M > G_BM || N <= 0 || K <= 0) return 0;
     const int tiles = (N + BN - 1) / BN, num_k = (K + G_BK - 1) / G_BK;
-    int S = 128 / tiles;
+    int S = num_sms / tiles;
     if (S > 8) S = 8;
     if (S > num_k) S = num_k;
     while (S >= 2 && tiles > splitk_max_clusters<BN>(S)) --S;
@@ -1220,16 +1235,27 @@ int splitk_plan(int M, int N, int K, int* kb_per) {
 }
 
 template <int BN>
-cudaError_t launch_splitk(const CUtensorMap& tA, const CUtensorMap& tW, const void* bias,
+cudaError_t launch_splitk(const void* A, int64_t lda, const CUtensorMap& tW, const void* bias,
                           const void* R, int64_t ldr, void* C, int64_t ldc, int M, int N, int K,
                           int S, int kb_per, int* status, cudaStream_t stream) {
+    // A in boxes of only the rows that exist (rounded up to 8: whole 128-byte swizzle atoms)
+    const int a_rows = (M + 7) & ~7;
+    CUtensorMap tA;
+    {
+        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)lda * 2};
+        const uint32_t box[2] = {G_BK, (uint32_t)a_rows};
+        if (!encode_tmap_bf16(&tA, A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    const int nst = splitk_stages<BN>(a_rows);
+    const int smem = nst * (a_rows * 128 + G_BK * BN * 2) + SK_SMEM_EXTRA;
     cudaError_t err = cudaFuncSetAttribute(gemm_bf16_splitk_kernel<BN>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, sk_smem<BN>());
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_MAX);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + BN - 1) / BN, S);
     cfg.blockDim = dim3(G_THREADS);
-    cfg.dynamicSmemBytes = sk_smem<BN>();
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1243,7 +1269,7 @@ cudaError_t launch_splitk(const CUtensorMap& tA, const CUtensorMap& tW, const vo
     return cudaLaunchKernelEx(&cfg, gemm_bf16_splitk_kernel<BN>, tA, tW,
                               reinterpret_cast<const __nv_bfloat16*>(bias),
                               reinterpret_cast<const __nv_bfloat16*>(R), ldr,
-                              static_cast<__nv_bfloat16*>(C), ldc, M, N, K, kb_per, status);
+                              static_cast<__nv_bfloat16*>(C), ldc, M, N, K, kb_per, a_rows, nst, status);
 }
 
 }  // namespace
@@ -1362,10 +1388,10 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
     // measured 1-20% faster from 32 rows up, the same at one row.  Past 64 such tiles (N >
     // 8192) 256-column tiles still leave room for clusters of two.
     int kb_per = 0;
-    int S = splitk_plan<128>(M, N, K, &kb_per);
-    if (S > 0) return launch_splitk<128>(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
-    S = splitk_plan<256>(M, N, K, &kb_per);
-    if (S > 0) return launch_splitk<256>(tA, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
+    int S = splitk_plan<128>(M, N, K, num_sms, &kb_per);
+    if (S > 0) return launch_splitk<128>(A, lda, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
+    S = splitk_plan<256>(M, N, K, num_sms, &kb_per);
+    if (S > 0) return launch_splitk<256>(A, lda, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);
     cudaError_t err = cudaFuncSetAttribute(tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
     if (err != cudaSuccess) return err;

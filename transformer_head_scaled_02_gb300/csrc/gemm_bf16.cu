@@ -371,6 +371,66 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 // Partial layout: row r at r * BN * 4 bytes, its BN / 4 groups of four columns as float4s,
 // the low three bits of the group index XORed with r & 7 so that the eight rows a
 // quarter-warp writes hit different banks.
+// One rank's share of the split kernel's reduction: column groups [g0, g0 + w) of rows [0, M),
+// each the sum of the S partials in rank order (+ bias, + residual), written to C.  A thread
+// takes U elements at a time and has all their U x S loads from distributed shared memory in
+// flight before it adds any: each load is a round trip of several hundred cycles.
+template <int S, int BN>
+__device__ __forceinline__ void splitk_reduce(uint32_t sPart, int g0, int w, int M, int N, int n0,
+                                              const __nv_bfloat16* __restrict__ bias,
+                                              const __nv_bfloat16* __restrict__ R, int64_t ldr,
+                                              __nv_bfloat16* __restrict__ C, int64_t ldc) {
+    constexpr int U = S <= 2 ? 8 : (S <= 4 ? 4 : 2);  // at most 64 registers of loads
+    const int count = M * w;
+#pragma unroll 1
+    for (int e0 = threadIdx.x; e0 < count; e0 += U * G_THREADS) {
+        float4 p[U][S];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * G_THREADS;
+            if (e < count) {
+                const int row = e / w;
+                const int g = g0 + e % w;
+                const uint32_t off = (uint32_t)(row * BN * 4) + ((uint32_t)((g & ~7) | ((g ^ row) & 7)) << 4);
+#pragma unroll
+                for (int r = 0; r < S; ++r) p[u][r] = ld_shared_cluster_v4(mapa_shared(sPart + off, (uint32_t)r));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * G_THREADS;
+            if (e >= count) break;
+            const int row = e / w;
+            const int n = n0 + (g0 + e % w) * 4;
+            if (n >= N) continue;  // N is a multiple of 8: a group of four is all in or out
+            float4 acc = p[u][0];
+#pragma unroll
+            for (int r = 1; r < S; ++r) {
+                acc.x += p[u][r].x;
+                acc.y += p[u][r].y;
+                acc.z += p[u][r].z;
+                acc.w += p[u][r].w;
+            }
+            if (bias != nullptr) {
+                const uint2 bb = *reinterpret_cast<const uint2*>(bias + n);
+                acc.x += __uint_as_float(bb.x << 16);
+                acc.y += __uint_as_float(bb.x & 0xffff0000u);
+                acc.z += __uint_as_float(bb.y << 16);
+                acc.w += __uint_as_float(bb.y & 0xffff0000u);
+            }
+            if (R != nullptr) {
+                const uint2 rr = *reinterpret_cast<const uint2*>(R + (int64_t)row * ldr + n);
+                acc.x += __uint_as_float(rr.x << 16);
+                acc.y += __uint_as_float(rr.x & 0xffff0000u);
+                acc.z += __uint_as_float(rr.y << 16);
+                acc.w += __uint_as_float(rr.y & 0xffff0000u);
+            }
+            *reinterpret_cast<uint2*>(C + (int64_t)row * ldc + n) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(G_THREADS, 1)
     gemm_bf16_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -521,45 +581,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tc_fence_before();
     cluster_sync_all();
     {
-        // ---------------- reduction of this rank's column groups [g0, g1) over the S partials
+        // ---------------- reduction of this rank's column groups [g0, g0 + w) over the S partials
         const int gs = (GROUPS + S - 1) / S;
         const int g0 = rank * gs;
         const int w = min(GROUPS, g0 + gs) - g0;
-        const int count = w > 0 ? M * w : 0;
-#pragma unroll 1
-        for (int e = threadIdx.x; e < count; e += G_THREADS) {
-            const int row = e / w;
-            const int g = g0 + e % w;
-            const int n = n0 + g * 4;
-            if (n >= N) continue;  // N is a multiple of 8: a group of four is all in or out
-            const uint32_t off = (uint32_t)(row * BN * 4) + ((uint32_t)((g & ~7) | ((g ^ row) & 7)) << 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                if (r < S) {
-                    const float4 p = ld_shared_cluster_v4(mapa_shared(sPart + off, (uint32_t)r));
-                    acc.x += p.x;
-                    acc.y += p.y;
-                    acc.z += p.z;
-                    acc.w += p.w;
-                }
+        if (w > 0) {
+            switch (S) {
+                case 2: splitk_reduce<2, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                case 3: splitk_reduce<3, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                case 4: splitk_reduce<4, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                case 5: splitk_reduce<5, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                case 6: splitk_reduce<6, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                case 7: splitk_reduce<7, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
+                default: splitk_reduce<8, BN>(sPart, g0, w, M, N, n0, bias, R, ldr, C, ldc); break;
             }
-            if (bias != nullptr) {
-                const uint2 bb = *reinterpret_cast<const uint2*>(bias + n);
-                acc.x += __uint_as_float(bb.x << 16);
-                acc.y += __uint_as_float(bb.x & 0xffff0000u);
-                acc.z += __uint_as_float(bb.y << 16);
-                acc.w += __uint_as_float(bb.y & 0xffff0000u);
-            }
-            if (R != nullptr) {
-                const uint2 rr = *reinterpret_cast<const uint2*>(R + (int64_t)row * ldr + n);
-                acc.x += __uint_as_float(rr.x << 16);
-                acc.y += __uint_as_float(rr.x & 0xffff0000u);
-                acc.z += __uint_as_float(rr.y << 16);
-                acc.w += __uint_as_float(rr.y & 0xffff0000u);
-            }
-            *reinterpret_cast<uint2*>(C + (int64_t)row * ldc + n) =
-                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
         }
     }
     __syncwarp();

@@ -128,6 +128,22 @@ def test_residual_forward(dtype, d):
     assert_close(got, ref, dtype, f"residual d={d}")
 
 
+@pytest.mark.parametrize("B,T,d,h_kv,gated,causal", [
+    (1, 100, 64, 4, False, True),    # 100 rows: both projections split K over clusters
+    (2, 64, 128, 2, True, False),    # 128 rows, grouped heads and the gate
+    (3, 5, 64, 1, False, True),      # 15 rows (a decode-sized batch), one K/V head
+])
+def test_few_row_forward_with_residual(B, T, d, h_kv, gated, causal):
+    """Forwards of at most 128 rows: the projections (the output one with the residual in its
+    epilogue) take the few-row split kernel; the whole layer equals the oracle's."""
+    h = 4
+    D = h * d
+    x = _inputs(70, "bf16", B, T, D, h, d, h_kv, gated)
+    got = _gpu_forward(x, "bf16", D, h, d, h_kv, gated, causal, True)
+    ref = _oracle_forward(x, h, d, h_kv, gated, causal, True)
+    assert_close(got, ref, "bf16", f"few-row forward B={B} T={T} d={d}")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_residual_in_place_and_as_input(dtype):
     """residual == out (in place) and residual == X_q (the pages' X' = X + O W_O)."""

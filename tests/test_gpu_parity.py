@@ -108,6 +108,34 @@ def test_linear_step_bf16_few_rows(M, K, N, residual):
     assert torch.equal(C1, C2), "a second call gave a different result"
 
 
+@pytest.mark.parametrize("M,K,N,residual", [
+    (128, 1024, 1024, False),   # 32 tiles: K over clusters of 8
+    (1024, 512, 512, True),     # 128 tiles: clusters of 4 (the fp32 causal output projection)
+    (100, 296, 200, True),      # ragged K over 4 ranks (10 slices of 32: 3 + 3 + 3 + 1)
+    (70, 517, 45, False),       # unaligned rows; 17 slices over 8 ranks, the last two empty
+])
+def test_linear_step_f32_split(M, K, N, residual):
+    """fp32 projections with no more 64 x 64 tiles than SMs split K over clusters whose fp32
+    partial tiles are added in rank order through distributed shared memory: C = A W + bias
+    (+ R) equals the oracle's, the same bits on a second call."""
+    A = wl.random_tensor((M, K), seed=51, dtype="f32")
+    W = wl.random_tensor((K, N), seed=52, dtype="f32", scale=0.05)
+    b = wl.random_tensor((N,), seed=53, dtype="f32", scale=0.1)
+    R = wl.random_tensor((M, N), seed=54, dtype="f32") if residual else None
+    layer = Mha(64, 1, 64, dtype=torch.float32)
+    layer.ensure_workspace(1, 1, 1)
+    Ad, Wd, bd, Rd = (to_device(t, "f32") for t in (A, W, b, R))
+    C1 = layer.linear(Ad, Wd, bd, residual=Rd)
+    C2 = layer.linear(Ad, Wd, bd, residual=Rd)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    ref = oracle.linear(A, W, b)
+    if residual:
+        ref = ref + R.astype(np.float64)
+    assert_close(to_host(C1), ref, "f32", f"f32 split linear {M}x{K}x{N}")
+    assert torch.equal(C1, C2), "a second call gave a different result"
+
+
 @pytest.mark.parametrize("M,K,N", [(70, 37, 45), (129, 130, 67), (64, 33, 64)])
 def test_linear_step_f32_unaligned(M, K, N):
     """fp32 projections whose row strides are not a multiple of four floats take the scalar

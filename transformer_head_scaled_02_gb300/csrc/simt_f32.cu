@@ -31,11 +31,17 @@ constexpr int F_BN = 64;
 // (k = 0, 1, ...) with one fma per product.  VEC: A and W 16-byte aligned with row strides a
 // multiple of 4 floats, so that four consecutive elements of a row are one 16-byte global
 // load.
-template <int BK, bool VEC>
+//
+// SPLIT: a cluster of gridDim.z CTAs (2, 4 or 8) shares each tile, rank z multiplying the K slices
+// [z * kper, (z + 1) * kper); the fp32 partial tiles meet in distributed shared memory, where
+// rank z adds rows [z * 64 / S, (z + 1) * 64 / S) of all S partials in rank order (so the sum
+// does not depend on timing), then bias and residual, and writes C.  For grids of too few tiles
+// to keep several warps per scheduler busy.
+template <int BK, bool VEC, bool SPLIT>
 __global__ void __launch_bounds__(128)
     gemm_f32_kernel(const float* __restrict__ A, int64_t lda, const float* __restrict__ W,
                     int64_t ldw, const float* __restrict__ bias, const float* R, int64_t ldr,
-                    float* C, int64_t ldc, int M, int N, int K) {
+                    float* C, int64_t ldc, int M, int N, int K, int kper) {
     constexpr int BM = 64, THREADS = 128;
     constexpr int NA = BM * BK / 4 / THREADS;  // 4-element pieces of A per thread and slice
     constexpr int NW = BK * F_BN / 4 / THREADS;
@@ -47,32 +53,34 @@ __global__ void __launch_bounds__(128)
     const int ty = tid >> 4;
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * F_BN;
+    const int kbeg = SPLIT ? (int)blockIdx.z * kper : 0;
+    const int kend = SPLIT ? min(K, kbeg + kper) : K;  // loads past kend read as zeros
     float ra[NA][4], rw[NW][4];
     auto load = [&](int k0) {
 #pragma unroll
         for (int c = 0; c < NA; ++c) {
             const int idx = tid + c * THREADS;
             const int gm = m0 + idx / (BK / 4), gk = k0 + (idx % (BK / 4)) * 4;
-            if (VEC && gm < M && gk + 3 < K) {
+            if (VEC && gm < M && gk + 3 < kend) {
                 const float4 v = *reinterpret_cast<const float4*>(A + (int64_t)gm * lda + gk);
                 ra[c][0] = v.x; ra[c][1] = v.y; ra[c][2] = v.z; ra[c][3] = v.w;
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    ra[c][i] = (gm < M && gk + i < K) ? A[(int64_t)gm * lda + gk + i] : 0.f;
+                    ra[c][i] = (gm < M && gk + i < kend) ? A[(int64_t)gm * lda + gk + i] : 0.f;
             }
         }
 #pragma unroll
         for (int c = 0; c < NW; ++c) {
             const int idx = tid + c * THREADS;
             const int gw = k0 + idx / 16, gn = n0 + (idx % 16) * 4;
-            if (VEC && gw < K && gn + 3 < N) {
+            if (VEC && gw < kend && gn + 3 < N) {
                 const float4 v = *reinterpret_cast<const float4*>(W + (int64_t)gw * ldw + gn);
                 rw[c][0] = v.x; rw[c][1] = v.y; rw[c][2] = v.z; rw[c][3] = v.w;
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    rw[c][i] = (gw < K && gn + i < N) ? W[(int64_t)gw * ldw + gn + i] : 0.f;
+                    rw[c][i] = (gw < kend && gn + i < N) ? W[(int64_t)gw * ldw + gn + i] : 0.f;
             }
         }
     };
@@ -97,12 +105,12 @@ __global__ void __launch_bounds__(128)
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    load(0);
+    load(kbeg);
     store(0);
     __syncthreads();
     int buf = 0;
-    for (int k0 = 0; k0 < K; k0 += BK) {
-        const bool more = k0 + BK < K;
+    for (int k0 = kbeg; k0 < kend; k0 += BK) {
+        const bool more = k0 + BK < kend;
         if (more) load(k0 + BK);  // in flight while this slice is multiplied
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
@@ -124,6 +132,47 @@ __global__ void __launch_bounds__(128)
         if (more) store(buf ^ 1);  // the other buffer was last read before the previous barrier
         __syncthreads();
         buf ^= 1;
+    }
+    if constexpr (SPLIT) {
+        // the partial tile, row-major 64 x 64, over the A buffers (free after the last barrier)
+        float* part = &As[0][0][0];
+        static_assert(sizeof(As) >= BM * F_BN * sizeof(float), "partial tile does not fit");
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(part + (ty * 8 + i) * F_BN + tx * 4) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        cluster_sync_all();
+        const int S = (int)gridDim.z;
+        const int rank = (int)cluster_ctarank();
+        const int rows = BM / S;  // S divides 64
+        const uint32_t pbase = smem_u32(part);
+        for (int e = tid; e < rows * (F_BN / 4); e += THREADS) {
+            const int r = rank * rows + e / (F_BN / 4);
+            const int c4 = (e % (F_BN / 4)) * 4;
+            const uint32_t off = pbase + (uint32_t)((r * F_BN + c4) * 4);
+            float4 sum = ld_shared_cluster_v4(mapa_shared(off, 0));
+            for (int z = 1; z < S; ++z) {
+                const float4 p = ld_shared_cluster_v4(mapa_shared(off, (uint32_t)z));
+                sum.x += p.x;
+                sum.y += p.y;
+                sum.z += p.z;
+                sum.w += p.w;
+            }
+            const int gm = m0 + r;
+            if (gm < M) {
+                const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int gn = n0 + c4 + j;
+                    if (gn < N)
+                        C[(int64_t)gm * ldc + gn] =
+                            v[j] + (bias ? bias[gn] : 0.f) + (R ? R[(int64_t)gm * ldr + gn] : 0.f);
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();  // every partial stays until its readers are done
+        return;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -481,13 +530,45 @@ cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t
                             int M, int N, int K, cudaStream_t stream) {
     // 32-wide K slices: 16-wide ones measured slower on the 1024 x 512 x {1536, 512}
     // projections of the fp32 causal workload (43.7 / 28.4 against 42.4 / 20.3 us)
+    constexpr int BK = 32;
     const dim3 grid((unsigned)((N + F_BN - 1) / F_BN), (unsigned)((M + 63) / 64));
     const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0) &&
                      lda % 4 == 0 && ldw % 4 == 0;
+    // no more tiles than SMs: split K over clusters of 4, of 8 up to half as many tiles as
+    // SMs (measured on 64-1024 rows: 8 beats 4 beats 2 wherever all CTAs stay resident, 2 lost
+    // 4% at 240 tiles), each rank at least two K slices
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
+    const int64_t tiles = (int64_t)grid.x * grid.y;
+    const int slices = (K + BK - 1) / BK;
+    int S = 1;
+    if (tiles <= (int64_t)sms) S = tiles * 2 <= (int64_t)sms ? 8 : 4;
+    while (S > 1 && slices < 2 * S) S /= 2;
+    if (S > 1) {
+        const int kper = (slices + S - 1) / S * BK;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid.x, grid.y, (unsigned)S);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)S;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return vec ? cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, true, true>, A, lda, W, ldw, bias, R, ldr, C,
+                                        ldc, M, N, K, kper)
+                   : cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, false, true>, A, lda, W, ldw, bias, R, ldr, C,
+                                        ldc, M, N, K, kper);
+    }
     if (vec)
-        gemm_f32_kernel<32, true><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+        gemm_f32_kernel<BK, true, false><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, K);
     else
-        gemm_f32_kernel<32, false><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K);
+        gemm_f32_kernel<BK, false, false><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, K);
     return cudaGetLastError();
 }
 

@@ -5,14 +5,18 @@
 // itwiki.kr "멀티 헤드 어텐션", tensor-shape table rows 투영 and 출력 투영, and the residual
 // form X' = X + O W_O of iamjaehka13.blog "[Deep Learning 5] Attention의 내부 계산", section 14.
 //
-// Three persistent, warp-specialised kernels (the host picks one per shape):
-//   gemm_bf16_tc_kernel     M <= 128: one CTA per SM, 128 x 256 tiles;
-//   gemm_bf16_pair_kernel   CTA pairs (cta_group::2), 256 x 256 tiles; optionally a second,
-//                           independent projection in the same grid (cross-attention's query
-//                           side next to its key / value side);
+// Four warp-specialised kernels (the host picks one per shape):
+//   gemm_bf16_splitk_kernel M <= 128 (a decode step's tokens): clusters of CTAs split K over
+//                           128 x 128 tiles (128 x 256 past 64 such tiles) and add their fp32
+//                           partials through distributed shared memory;
+//   gemm_bf16_tc_kernel     M <= 128 where no split applies: one CTA per SM, persistent over
+//                           128 x 256 tiles;
+//   gemm_bf16_pair_kernel   CTA pairs (cta_group::2), 256 x 256 tiles, persistent; optionally
+//                           a second, independent projection in the same grid
+//                           (cross-attention's query side next to its key / value side);
 //   gemm_bf16_pairT_kernel  CTA pairs with the accumulator transposed, 192 x 256 tiles, where
 //                           their rounds over the pairs cost less.
-// Roles, as in the first:
+// Roles, as in the one-CTA kernel:
 //   warp 0      TMA producer: A tile 128x64 (K-major, 128B swizzle) and W tile 64x256
 //               (N-major: four 64x64 boxes) into a 4-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N=256, K=16)

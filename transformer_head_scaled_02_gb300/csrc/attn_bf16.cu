@@ -44,6 +44,8 @@
 // rescale O and l.  Every exponential runs on the MUFU unit (ex2.approx), which retires 32
 // results per clock per SM on GB300 -- a key tile's 32768 exponentials in 1024 clocks, within
 // the tensor core's time for the same tile.
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -985,13 +987,15 @@ cudaError_t launch_attn_d64(const void* Q, int64_t ldq, const void* K, int64_t l
     const bool sorted = kv_lengths != nullptr && !causal && B <= D64_SORT_MAX_B;
     auto kernel = G != nullptr ? (sorted ? attn_bf16_d64_kernel<true, true> : attn_bf16_d64_kernel<true, false>)
                                : (sorted ? attn_bf16_d64_kernel<false, true> : attn_bf16_d64_kernel<false, false>);
-    static int pool_ok[4] = {-1, -1, -1, -1};
-    int& ok = pool_ok[(G != nullptr ? 2 : 0) + (sorted ? 1 : 0)];
+    static std::atomic<int> pool_ok[4] = {{-1}, {-1}, {-1}, {-1}};
+    std::atomic<int>& slot = pool_ok[(G != nullptr ? 2 : 0) + (sorted ? 1 : 0)];
+    int ok = slot.load(std::memory_order_relaxed);
     if (ok < 0) {
         cudaFuncAttributes fa;
         const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
         ok = fa.numRegs * D64_THREADS >= 128 * (D64_REGS_CTRL + D64_REGS_SOFTMAX) ? 1 : 0;
+        slot.store(ok, std::memory_order_relaxed);
     }
     if (!ok) return cudaErrorInvalidConfiguration;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D64_SMEM);

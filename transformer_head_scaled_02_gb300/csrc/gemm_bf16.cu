@@ -28,6 +28,8 @@
 // W stays in its natural (in,out) layout: the MMA reads it as an MN-major operand, so no
 // transpose pass over the weights is needed.  Ragged M, N, K are handled by TMA bounds
 // (zero fill on loads, clipping on stores).
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -1174,10 +1176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 // grid's size.
 template <typename Kernel>
 int pair_occupancy(Kernel kernel, int variant, int num_sms) {
-    static int cache[3][64] = {{0}};
+    static std::atomic<int> cache[3][64];  // 0 until asked
     int dev = 0;
     cudaGetDevice(&dev);
-    int n = dev >= 0 && dev < 64 ? cache[variant][dev] : 0;
+    int n = dev >= 0 && dev < 64 ? cache[variant][dev].load(std::memory_order_relaxed) : 0;
     if (n > 0) return n;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
@@ -1191,7 +1193,7 @@ int pair_occupancy(Kernel kernel, int variant, int num_sms) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
-    if (dev >= 0 && dev < 64) cache[variant][dev] = n;
+    if (dev >= 0 && dev < 64) cache[variant][dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -1225,10 +1227,10 @@ int splitk_stages(int a_rows) {
 // tile width and S.
 template <int BN>
 int splitk_max_clusters(int S) {
-    static int cache[64][9];  // count + 1; 0 = not asked yet
+    static std::atomic<int> cache[64][9];  // count + 1; 0 = not asked yet
     int dev = -1;
     if (S < 1 || S > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    int& c = cache[dev][S];
+    int c = cache[dev][S].load(std::memory_order_relaxed);
     if (c == 0) {
         int n = 0;
         if (cudaFuncSetAttribute(gemm_bf16_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1248,6 +1250,7 @@ int splitk_max_clusters(int S) {
         }
         cudaGetLastError();
         c = n + 1;
+        cache[dev][S].store(c, std::memory_order_relaxed);
     }
     return c - 1;
 }
@@ -1354,10 +1357,10 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
         // 0.91 of a 256-row one (measured: c3's QKV projection, 7 rounds of 192-row tiles
         // against 6 of 256-row ones, 41.1 against 38.8 us; M = 8192, N = K = 768, 2 rounds
         // each, 15.1 against 16.9 us)
-        static int t_pairs_cache[64] = {0};
+        static std::atomic<int> t_pairs_cache[64];  // 0 until asked
         int dev = 0;
         cudaGetDevice(&dev);
-        int t_pairs = dev >= 0 && dev < 64 ? t_pairs_cache[dev] : 0;
+        int t_pairs = dev >= 0 && dev < 64 ? t_pairs_cache[dev].load(std::memory_order_relaxed) : 0;
         if (t_pairs == 0) {
             if (cudaFuncSetAttribute(gemm_bf16_pairT_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      T_SMEM) != cudaSuccess)
@@ -1377,7 +1380,7 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
             if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_pairT_kernel, &cfg) != cudaSuccess || n <= 0)
                 n = num_sms / 2;
             t_pairs = n;
-            if (dev >= 0 && dev < 64) t_pairs_cache[dev] = n;
+            if (dev >= 0 && dev < 64) t_pairs_cache[dev].store(n, std::memory_order_relaxed);
         }
         const int64_t nb = (N + G_BN - 1) / G_BN;
         const int64_t tiles_t = ((M + T_BM - 1) / T_BM) * nb, tiles_s = ((M + 255) / 256) * nb;

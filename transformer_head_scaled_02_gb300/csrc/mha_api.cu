@@ -19,6 +19,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "../../include/mha.h"
 #include "internal.h"
 
@@ -26,23 +28,25 @@ namespace mha {
 
 // ------------------------------------------------------------------ tensor maps
 
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static int g_encode_state = 0;  // 0 unknown, 1 ok, -1 unavailable
+// The driver's tensor-map encoder, looked up once (host threads may race to do it: the
+// lookups agree, and the pointer is published before the state that says it is there).
+static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
+static std::atomic<int> g_encode_state{0};  // 0 unknown, 1 ok, -1 unavailable
 
 static bool get_encoder() {
-    if (g_encode_state == 0) {
+    if (g_encode_state.load(std::memory_order_acquire) == 0) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
         const cudaError_t err =
             cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
         if (err == cudaSuccess && q == cudaDriverEntryPointSuccess && fn != nullptr) {
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-            g_encode_state = 1;
+            g_encode.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn), std::memory_order_relaxed);
+            g_encode_state.store(1, std::memory_order_release);
         } else {
-            g_encode_state = -1;
+            g_encode_state.store(-1, std::memory_order_release);
         }
     }
-    return g_encode_state == 1;
+    return g_encode_state.load(std::memory_order_acquire) == 1;
 }
 
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
@@ -59,7 +63,7 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
         estr[i] = 1;
         if (i + 1 < rank) gstr[i] = strides_bytes[i];
     }
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+    const CUresult r = g_encode.load(std::memory_order_relaxed)(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                                 const_cast<void*>(base), gdim, gstr, bdim, estr,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -121,20 +125,18 @@ WsLayout ws_layout(const mha_s* m, int B, int T_q, int T_kv) {
     return w;
 }
 
-int g_num_sms = 0;
-int g_num_sms_dev = -1;
+std::atomic<int> g_num_sms[64];  // SM count per device, 0 until asked
 
 mha_status query_sms(int* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
-    if (dev != g_num_sms_dev) {
-        int n = 0;
+    int n = dev >= 0 && dev < 64 ? g_num_sms[dev].load(std::memory_order_relaxed) : 0;
+    if (n <= 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             return MHA_ERR_CUDA;
-        g_num_sms = n;
-        g_num_sms_dev = dev;
+        if (dev >= 0 && dev < 64) g_num_sms[dev].store(n, std::memory_order_relaxed);
     }
-    *out = g_num_sms;
+    *out = n;
     return MHA_OK;
 }
 

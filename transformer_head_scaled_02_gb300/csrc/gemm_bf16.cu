@@ -7,8 +7,9 @@
 //
 // Four warp-specialised kernels (the host picks one per shape):
 //   gemm_bf16_splitk_kernel M <= 128 (a decode step's tokens): clusters of CTAs split K over
-//                           128 x 128 tiles (128 x 256 past 64 such tiles) and add their fp32
-//                           partials through distributed shared memory;
+//                           128 x 128 tiles (128 x 256 where clusters of two over the narrow
+//                           ones would not all fit at once) and add their fp32 partials
+//                           through distributed shared memory;
 //   gemm_bf16_tc_kernel     M <= 128 where no split applies: one CTA per SM, persistent over
 //                           128 x 256 tiles;
 //   gemm_bf16_pair_kernel   CTA pairs (cta_group::2), 256 x 256 tiles, persistent; optionally

@@ -1428,8 +1428,10 @@ cudaError_t launch_gemm_bf16(const void* A, int64_t lda, const void* W, int64_t 
     }
     // few rows: clusters of S CTAs split K over 128-column tiles (every row is written, seg_len
     // or not).  128 columns rather than 256: each rank exchanges half the partial bytes, and
-    // measured 1-20% faster from 32 rows up, the same at one row.  Past 64 such tiles (N >
-    // 8192) 256-column tiles still leave room for clusters of two.
+    // measured 1-20% faster from 32 rows up, the same at one row, and still faster where
+    // 256-column tiles would allow more CTAs (32 x 2048 x 6144: 11.6 against 12.1 us).  Where
+    // clusters of two over 128-column tiles would not all fit at once (N > 9728 on 152 SMs),
+    // 256-column tiles still leave room for them.
     int kb_per = 0;
     int S = splitk_plan<128>(M, N, K, num_sms, &kb_per);
     if (S > 0) return launch_splitk<128>(A, lda, tW, bias, R, ldr, C, ldc, M, N, K, S, kb_per, status, stream);

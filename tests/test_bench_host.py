@@ -72,3 +72,45 @@ def test_max_over_ranks_gloo_world2():
         assert p.exitcode == 0
     got = dict(q.get() for _ in range(2))
     assert got == {0: 15.0, 1: 15.0}
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_launch_count_per_forward():
+    """gpu_launches counts three kernels per self-attention forward; cross-attention pairs its
+    two projections in one bf16 launch only when both have more than 128 rows."""
+    bench = _bench_module()
+    from transformer_head_scaled_02_gb300 import workloads as wl
+    assert bench.launches_per_step(wl.WORKLOADS["c3_bf16_causal"]) == 3
+    assert bench.launches_per_step(wl.WORKLOADS["c5_bf16_cross"]) == 3
+    few = wl.custom("few_q", B=2, T_q=64, T_kv=300, D=256, h=4, d_k=64, cross=True)
+    assert bench.launches_per_step(few) == 4
+    f32 = wl.custom("f32_cross", B=2, T_q=200, T_kv=300, D=64, h=4, d_k=16, dtype="f32", cross=True)
+    assert bench.launches_per_step(f32) == 4
+
+
+def test_step_percentiles():
+    bench = _bench_module()
+    s = bench.step_stats([0.1 * i for i in range(1, 11)])   # 0.1 .. 1.0
+    assert s == {"p10": 0.19, "median": 0.55, "p90": 0.91}
+
+
+def test_recorded_traffic_only_for_the_profiled_source(monkeypatch):
+    """A DRAM figure is reported only while the kernel's source file hashes to the value the
+    capture was taken on; any other source gives None."""
+    bench = _bench_module()
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        d = json.load(f)
+    e = d["c3_bf16_causal"]["attention"]
+    assert bench.recorded_traffic("attention", "c3_bf16_causal", "attn_bf16.cu") == \
+        (e["dram_bytes_per_launch"] if e["source_sha256_16"] == bench.kernel_source_hash("attn_bf16.cu")
+         else None)
+    assert bench.recorded_traffic("attention", "no_such_workload", "attn_bf16.cu") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda fname: "0" * 16)
+    assert bench.recorded_traffic("attention", "c3_bf16_causal", "attn_bf16.cu") is None

@@ -1,6 +1,7 @@
 """Host-side logic of bench.py, on CPU: the reference arm's JSON line, the
-non-zero ranks of a multi-rank launch, and the max-over-ranks reduction of the
-timed region (gloo, world size 2)."""
+non-zero ranks of a multi-rank launch, the max-over-ranks reduction of the
+timed region (gloo, world size 2), the kernel count per forward, the step
+percentiles and the source-hash gate on recorded DRAM traffic."""
 import json
 import os
 import subprocess

@@ -76,7 +76,7 @@ struct DtcCfg {
     static constexpr int CH = HD / 64;                   // 64-column chunks of a row
     static constexpr int CHUNK = 128 * 128;              // 128 rows x 64 bf16 = 16 KB
     static constexpr int TILE = CH * CHUNK;              // one Q, K or V tile
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = HD == 128 ? 3 : 2;  // d = 64 keeps two CTAs per SM
     static constexpr int SMEM = TILE + 2 * STAGES * TILE + 256 + 1024;
     static constexpr uint32_t TMEM_COLS = HD == 64 ? 256 : 512;
     static constexpr uint32_t S_COL = 0, O_COL = 128, P_COL = 128 + HD;

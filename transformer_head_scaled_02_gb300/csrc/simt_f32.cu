@@ -560,10 +560,13 @@ cudaError_t launch_gemm_f32(const float* A, int64_t lda, const float* W, int64_t
         attr[0].val.clusterDim.z = (unsigned)S;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return vec ? cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, true, true>, A, lda, W, ldw, bias, R, ldr, C,
-                                        ldc, M, N, K, kper)
-                   : cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, false, true>, A, lda, W, ldw, bias, R, ldr, C,
-                                        ldc, M, N, K, kper);
+        const cudaError_t err =
+            vec ? cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, true, true>, A, lda, W, ldw, bias, R, ldr, C, ldc,
+                                     M, N, K, kper)
+                : cudaLaunchKernelEx(&cfg, gemm_f32_kernel<BK, false, true>, A, lda, W, ldw, bias, R, ldr, C, ldc,
+                                     M, N, K, kper);
+        if (err == cudaSuccess) return err;
+        cudaGetLastError();  // no room for the clusters here: one CTA per tile below
     }
     if (vec)
         gemm_f32_kernel<BK, true, false><<<grid, 128, 0, stream>>>(A, lda, W, ldw, bias, R, ldr, C, ldc, M, N, K, K);

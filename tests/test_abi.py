@@ -161,6 +161,14 @@ def test_decode_and_linear_ex_reject_bad_arguments(lib):
         assert dec(bf, B=0) == L.MHA_OK and dec(bf, T_q=0) == L.MHA_OK
         assert L.mha_decode_workspace_size(bf, 2, 1, 1024) > 256
         assert L.mha_decode_workspace_size(None, 2, 1, 1024) == 0
+        # status 256 + one (max, sum, d values) fp32 record per (batch, query head, new token,
+        # split), splits at least two 128-key tiles long; 256-byte aligned
+        for B, Tq, Tmax in ((2, 1, 1024), (32, 1, 8192), (3, 4, 300)):
+            splits = (Tmax + 255) // 256
+            part = 4 * B * 16 * Tq * splits * (64 + 2)
+            assert L.mha_decode_workspace_size(bf, B, Tq, Tmax) == 256 + (part + 255) // 256 * 256
+        assert L.mha_decode_workspace_size(bf, 0, 1, 1024) == 256
+        assert L.mha_decode_workspace_size(bf, -1, 1, 1024) == 0
 
         def lin(**kw):
             a = dict(A=fake, lda=64, M=128, K=64, W=fake + (1 << 28), ldw=64, N=64, bias=None,
